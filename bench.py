@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the nanochat attention block on one B300 per rank.  Prints one JSON line (rank 0).
+
+A step is one pass of the prefill forward over the depth-12 SSSL layer pattern: four nc_attn_fwd calls (windows
+1024, 1024, 1024, 2048) on B=4, T=2048, Hq=Hkv=6, D=128, each layer with its own seeded q, k, v (seed = layer
+index), all resident in HBM.  L2 is flushed (512 MiB write) before every timed step, outside the timed events.
+Each call runs the RoPE + QK-norm prologue kernel and the tcgen05 attention kernel.
+
+value      in-band TFLOP/s of the whole job: 4 * D * N_vis(T, W) * B * Hq FLOPs per call, summed over the calls of
+           all ranks, divided by the device time of the slowest rank (CUDA events, max over ranks).
+roofline   the attention kernel (tensor-core bound): in-band FLOPs of its launches / their CUDA-event durations,
+           against the measured bf16 dense peak.
+decode     the KV-cache decode step (64 sequences, cache lengths U[1, 4096], Hq=12, Hkv=4, W=2048), GB/s of the
+           algorithmic bytes (K/V rows in the window, q, out, lengths, new rows) against the measured HBM peak;
+           four cache copies are rotated so that every call reads HBM.
+e2e        the same prefill metric through the public API with the inputs in pinned host memory: host-to-device
+           copies of q, k, v and the device-to-host copy of every output inside the timed region.
+cpu_baseline  the fp64 oracle on this machine's host cores on a bounded sample of the same workload.
+
+--impl reference times the oracle instead (the reference arm): each step is a bounded sample of the workload.
+With torchrun (WORLD_SIZE > 1) every rank runs an independent replica on its own GPU (weak scaling, no data-path
+collective); rank 0 prints.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from seeded_inputs import DECODE, DEPTH12, decode_inputs, fwd_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (in-band) & % bf16 peak; decode GB/s & % HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ---------------------------------------------------------------------------------------------------------- counts
+def n_vis(T, W):
+    """Visible (query, key) pairs of one (batch, head): sum over i of min(i, W) + 1 (all i + 1 when unbounded)."""
+    if W < 0 or W >= T - 1:
+        return T * (T + 1) // 2
+    return (W + 1) * (W + 2) // 2 + (T - 1 - W) * (W + 1)
+
+
+def fwd_flops(B, T, Hq, D, W):
+    """In-band FLOPs of one forward call: QK^T and PV, 2 * D each, over the visible pairs."""
+    return 4 * D * n_vis(T, W) * B * Hq
+
+
+def decode_bytes(lens, window, B, Hq, Hkv, D, with_new):
+    """Algorithmic HBM bytes of one decode call: the K and V rows in each window, q, out, the lengths, and (with a new
+    key) the new rows read and written into the cache."""
+    rows = 0
+    for p in lens:
+        L = p + (1 if with_new else 0)
+        lo = 0 if window < 0 else max(0, p - window)
+        rows += max(0, min(L, p) - lo)          # rows read from the cache (the new row comes from k_new / v_new)
+    b = rows * Hkv * D * 2 * 2
+    b += 2 * B * Hq * D * 2 + 4 * B
+    if with_new:
+        b += 2 * (B * Hkv * D * 2) * 2          # read k_new, v_new; write both into the cache
+    return b
+
+
+# --------------------------------------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons of the GPU during the timed region (NVML, else nvidia-smi)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x10: "sync_boost"}
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = None
+            try:
+                props = torch.cuda.get_device_properties(device_index)
+                bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+                h = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
+            except Exception:
+                h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self._nvml = pynvml
+            self._h = h
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self._nvml = None
+
+    def _run(self):
+        pn = self._nvml
+        while not self._stop.is_set():
+            try:
+                self.samples.append(pn.nvmlDeviceGetClockInfo(self._h, pn.NVML_CLOCK_SM))
+                self.reasons |= int(pn.nvmlDeviceGetCurrentClocksEventReasons(self._h))
+            except Exception:
+                try:
+                    self.reasons |= int(pn.nvmlDeviceGetCurrentClocksThrottleReasons(self._h))
+                except Exception:
+                    pass
+            time.sleep(0.002)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+        if not self.samples:
+            return self._smi_once()
+        names = sorted(n for bit, n in self.REASONS.items() if self.reasons & bit)
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(self.samples), "source": "nvml"}
+
+    @staticmethod
+    def _smi_once():
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                                  "--format=csv,noheader,nounits", "-i", "0"], capture_output=True, text=True,
+                                 timeout=20).stdout.strip().splitlines()[0].split(",")
+            return {"sm_mhz": float(out[0]), "sm_max_mhz": float(out[1]), "reasons": [out[2].strip()],
+                    "samples": 1, "source": "nvidia-smi after the timed region"}
+        except Exception as e:  # noqa: BLE001
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": str(e)}
+
+
+def kernel_traffic(kernel, src_files):
+    """DRAM bytes per launch from a committed ncu summary, when it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)[kernel]
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for f in src_files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    if d.get("source_sha256") != h.hexdigest():
+        return None
+    return d.get("bytes_per_launch")
+
+
+# -------------------------------------------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=ws)
+    return ws, rank, local
+
+
+def dist_max(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------------- CPU (oracle)
+def oracle_fwd_sample(batches=4):
+    """Times the fp64 oracle on `batches` batch rows of one W=1024 layer of the depth-12 workload."""
+    from oracle import ref
+    w = DEPTH12
+    q, k, v = (t[:batches].double().numpy() for t in fwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=0))
+    t0 = time.perf_counter()
+    ref.attn_fwd(q, k, v, 1024)
+    dt = time.perf_counter() - t0
+    flops = fwd_flops(batches, w.T, w.Hq, w.D, 1024)
+    return flops, dt
+
+
+def cpu_baseline():
+    flops, dt = oracle_fwd_sample(4)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"one W=1024 layer of the depth-12 workload (B=4, T=2048, Hq=Hkv=6), numpy fp64, "
+                      f"{flops / 1e9:.2f} in-band GFLOP in {dt:.2f} s on {cpu_model()} "
+                      f"({os.cpu_count()} logical cores)"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    flops_w, secs = [], []
+    for it in range(args.warmup + args.steps):
+        f, dt = oracle_fwd_sample(1)
+        if it >= args.warmup:
+            flops_w.append(f)
+            secs.append(dt)
+    value = sum(flops_w) / sum(secs) / 1e12
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "depth12_sssl_b4_t2048_h6: B=4 T=2048 Hq=Hkv=6 D=128, SSSL windows (1024,1024,1024,2048)",
+                   "reference_step": "batch row 0 of one W=1024 layer per step (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: batch row 0 of one W=1024 layer of the depth-12 workload, numpy fp64, "
+                                   f"{cpu_model()}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------------- GPU arm
+def run_ours(args, ws, rank, local):
+    from transformer_attention_06_b300 import nc_attn as nc
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    w = DEPTH12
+    layers = []
+    for li, W in enumerate(w.windows):
+        q, k, v = (t.to(dev) for t in fwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=li))
+        layers.append((q, k, v, torch.empty_like(q), W))
+    flops_layer = [fwd_flops(w.B, w.T, w.Hq, w.D, W) for W in w.windows]
+    flops_step = sum(flops_layer)
+    wsp = torch.empty(nc.nc_attn_fwd_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        for li, (q, k, v, o, W) in enumerate(layers):
+            nc.nc_attn_fwd(q, k, v, o, window=W, workspace=wsp, events=evs[li] if evs else None)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    step_ev = [(mk(), mk()) for _ in range(args.steps)]
+    k_ev = [[(mk(), mk(), mk()) for _ in layers] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    dist_barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        step_ev[s][0].record(stream)
+        step(k_ev[s])
+        step_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    dist_barrier(ws)
+    total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    total_ms_max = dist_max(total_ms, ws)
+    value = ws * args.steps * flops_step / (total_ms_max * 1e-3) / 1e12
+    k2_ms = [[e[1].elapsed_time(e[2]) for e in row] for row in k_ev]
+    k1_ms = [[e[0].elapsed_time(e[1]) for e in row] for row in k_ev]
+    k2_total = sum(sum(r) for r in k2_ms)
+    k2_flops = args.steps * flops_step
+    achieved = k2_flops / (k2_total * 1e-3) / 1e12
+    traffic = kernel_traffic("attn_fwd_kernel", ["transformer_attention_06_b300/csrc/attn_fwd.cuh",
+                                                 "transformer_attention_06_b300/csrc/common.cuh"])
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.skip_e2e:
+        host = [(q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory(), torch.empty_like(o, device="cpu").pin_memory())
+                for (q, k, v, o, W) in layers]
+        h2d = sum(x.numel() * x.element_size() for (q, k, v, _) in host for x in (q, k, v))
+        d2h = sum(o.numel() * o.element_size() for (_, _, _, o) in host)
+        n_e2e = max(3, min(args.steps, 10))
+        times = []
+        for it in range(2 + n_e2e):
+            a, b = mk(), mk()
+            a.record(stream)
+            for (hq, hk, hv, ho), (q, k, v, o, W) in zip(host, layers):
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                nc.nc_attn_fwd(q, k, v, o, window=W, workspace=wsp)
+                ho.copy_(o, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if it >= 2:
+                times.append(a.elapsed_time(b))
+        e2e_ms = dist_max(sum(times), ws)
+        e2e = {"value": ws * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    # ---- decode
+    dec = None
+    if not args.skip_decode:
+        dec = {}
+        dw = DECODE
+        for with_new in (False, True):
+            d = decode_inputs(dw.B, dw.Hq, dw.Hkv, dw.D, dw.Tcap, dw.len_lo, dw.len_hi, seed=0, with_new=with_new)
+            copies = [(d["kcache"].to(dev), d["vcache"].to(dev)) for _ in range(4)]
+            qd, lens = d["q"].to(dev), d["cache_lens"].to(dev)
+            kn = d["k_new"].to(dev) if with_new else None
+            vn = d["v_new"].to(dev) if with_new else None
+            out = torch.empty_like(qd)
+            dws = torch.zeros(nc.nc_attn_decode_workspace_bytes(dw.B, dw.Hq, dw.Hkv, dw.D, dw.Tcap, dw.window),
+                              dtype=torch.uint8, device=dev)
+            nbytes = decode_bytes(d["cache_lens"].tolist(), dw.window, dw.B, dw.Hq, dw.Hkv, dw.D, with_new)
+            n_dec = max(40, args.steps)
+            for i in range(max(3, args.warmup)):
+                kc, vc = copies[i % 4]
+                nc.nc_attn_decode(qd, kc, vc, lens, out, kn, vn, window=dw.window, workspace=dws)
+            torch.cuda.synchronize()
+            a, b = mk(), mk()
+            a.record(stream)
+            for i in range(n_dec):
+                kc, vc = copies[i % 4]
+                nc.nc_attn_decode(qd, kc, vc, lens, out, kn, vn, window=dw.window, workspace=dws)
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = dist_max(a.elapsed_time(b) * 1e3 / n_dec, ws)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            dec["with_new" if with_new else "cache_only"] = {
+                "value": gbs, "unit": "GB/s", "us_per_call": us, "bytes_per_call": nbytes,
+                "frac": gbs / peaks["hbm_gbs"], "calls": n_dec}
+            del copies
+            torch.cuda.empty_cache()
+        dec["config"] = (f"{dw.name}: B={dw.B} Hq={dw.Hq} Hkv={dw.Hkv} D={dw.D} Tcap={dw.Tcap} window={dw.window}, "
+                         f"cache lengths U[{dw.len_lo},{dw.len_hi}] seed 0; 4 rotated cache copies (> L2)")
+        dec["peak_gbs"] = peaks["hbm_gbs"]
+
+    st = nc.nc_attn_get_device_status(clear=True)
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hkv={w.Hkv} D={w.D}, one step = SSSL "
+                                   f"layers with windows {list(w.windows)}, distinct seeded q,k,v per layer",
+                       "l2": "512 MiB write before every timed step, outside the timed events",
+                       "flops_per_step": flops_step, "parallelism": f"replicas x{ws}"},
+            "frac_of_bf16_peak": value / ws / peaks["bf16_tflops"],
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                         "traffic": traffic, "peak_source": f"{peak_src} bf16 dense (burst)",
+                         "achieved_def": "sum of in-band FLOPs of the attention-kernel launches / sum of their "
+                                         "CUDA-event durations",
+                         "us_per_launch": 1e3 * k2_total / (args.steps * len(layers)),
+                         "prologue_us_per_launch": 1e3 * sum(sum(r) for r in k1_ms) / (args.steps * len(layers))},
+            "decode": dec,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps * len(layers) * 2,
+            "clocks": clk,
+            "device_status": nc.status_string(st),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,135 @@
+/* nc_attn -- the nanochat attention block on one B300 GPU (sm_103a), behind a plain C ABI.
+ *
+ * The block: half-split RoPE (base 100000) on q and k, then weightless RMSNorm of every q and k head vector
+ * (QK-norm), then causal grouped-query attention with an optional sliding window, scale 1/sqrt(D).
+ *   - "nanochat Admin & Developer Guide", section 3 "The GPT Model (Internals)": RoPE base theta 100000,
+ *     QK-norm, RMSNorm without learnable parameters, GQA with n_kv_head <= n_head, per-layer sliding windows
+ *     (window_pattern, passed to Flash Attention as (left, right) tuples).
+ *   - same guide, section 6 "Attention: FA3 with SDPA Fallback": the three masking cases (full causal,
+ *     single-token decode over a sliced KV window, windowed attention) and GQA.
+ *   - same guide, section 7 "The Inference Engine & Tool Use", "KV cache": cache tensors laid out
+ *     (B, T, H, D), positions tracked per row with an int32 cache_seqlens, new keys appended in place.
+ *   - "nanochat (Fucina port)", section "Architecture": half-split RoPE with an inverse-built table,
+ *     no-weight RMSNorm, grouped causal attention.
+ *
+ * Conventions for every entry point
+ *   - Tensors are bfloat16 (passed as void*, 16-bit storage), contiguous, row-major, in DEVICE memory owned by
+ *     the caller, and 16-byte aligned.  cache_lens is a device int32 array.
+ *   - D (head dim) must be 128; otherwise NC_ERR_UNSUPPORTED.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream) and never synchronizes.  Arguments are
+ *     checked on the host before anything is launched; an error return means nothing was launched.
+ *   - RoPE: element i of a head vector is paired with element i + D/2; theta_i = rope_base^(-2i/D); at
+ *     position t the pair is mapped to (x_i cos a + x_{i+D/2} sin a, -x_i sin a + x_{i+D/2} cos a), a = t theta_i.
+ *   - RMSNorm: y / sqrt(mean(y^2) + 1e-6), no weight, computed in fp32.
+ *   - window: -1 means unbounded (plain causal).  window >= 0 means key position j is visible to query position
+ *     i iff 0 <= i - j <= window (window + 1 keys including the query's own position).
+ *   - Arithmetic: bf16 operands, fp32 accumulation and softmax; the softmax probabilities are rounded to bf16
+ *     before the P.V product; outputs are rounded to bf16 (round to nearest even).
+ *   - Device-side problems never trap.  They set a sticky device status word that nc_attn_get_device_status()
+ *     returns: a bounded wait that ran out (NC_ERR_DEVICE_TIMEOUT) or a cache length outside the cache
+ *     (NC_ERR_DEVICE_BAD_INPUT; that row's output is written as zeros).
+ */
+#ifndef NC_ATTN_H
+#define NC_ATTN_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NC_OK = 0,
+  NC_ERR_INVALID_ARG = 1,      /* null / misaligned pointer, bad size, bad window or rope base */
+  NC_ERR_UNSUPPORTED = 2,      /* valid but not implemented here (D != 128, group size too large) */
+  NC_ERR_CUDA = 3,             /* a CUDA runtime / driver call or a kernel launch failed */
+  NC_ERR_DEVICE_TIMEOUT = 4,   /* a bounded wait inside a kernel ran out (see nc_attn_get_device_status) */
+  NC_ERR_DEVICE_BAD_INPUT = 5, /* a kernel found an invalid cache length (see nc_attn_get_device_status) */
+  NC_ERR_WORKSPACE = 6         /* the caller's workspace is null or smaller than the *_workspace_bytes value */
+} nc_status;
+
+/* ---- prefill / training forward ------------------------------------------------------------------------------
+ * q:[B,T,Hq,D]  k,v:[B,T,Hkv,D]  out:[B,T,Hq,D].  Token t of every sequence is at position t (0..T-1).
+ * Query head h uses kv head h / (Hq/Hkv).  Requires Hq % Hkv == 0, Hq/Hkv <= 128, T < 2^24.
+ *
+ * nc_attn_fwd_ws takes a caller-owned device workspace of at least nc_attn_fwd_workspace_bytes(...) bytes,
+ * 16-byte aligned, with no initial contents required; it holds the roped + normed q and k (bf16) between the
+ * two kernels and must not be used by another call until this one has finished on `stream`.
+ * nc_attn_fwd (the same call without a workspace argument) uses a workspace owned by the library, grown on
+ * demand with cudaMallocAsync on `stream`; it is for one stream at a time per device and must not be first
+ * called while `stream` is being captured into a CUDA graph.
+ */
+size_t nc_attn_fwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
+
+nc_status nc_attn_fwd_ws(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                         int D, int window, float rope_base, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                      int D, int window, float rope_base, cudaStream_t stream);
+
+/* Same as nc_attn_fwd_ws, and records CUDA events on `stream` around the two kernels it launches: `k1_begin`
+ * before the RoPE + QK-norm prologue, `k2_begin` between the prologue and the attention kernel, `k2_end` after the
+ * attention kernel.  Any event may be NULL.  Used to time each kernel with CUDA events on its own stream. */
+nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,
+                                int Hkv, int D, int window, float rope_base, void* workspace,
+                                size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin,
+                                cudaEvent_t k2_end, cudaStream_t stream);
+
+/* ---- the fused RoPE + QK-norm prologue alone -----------------------------------------------------------------
+ * qn = norm(rope(q)), kn = norm(rope(k)) at positions 0..T-1, bf16, same layouts as q and k.  This is the first
+ * kernel of nc_attn_fwd, exported so that the normalised vectors can be checked on their own.
+ */
+nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
+                              int D, float rope_base, cudaStream_t stream);
+
+/* ---- KV-cache single-token decode ------------------------------------------------------------------------------
+ * One new query token per sequence b, at position p_b = cache_lens[b].
+ *   q:[B,Hq,D]            raw query of the new token (roped at position p_b, then normed, inside the call)
+ *   kcache,vcache:[B,Tcap,Hkv,D]  rows 0..p_b-1 are used as given (already roped and normed)
+ *   cache_lens: device int32[B]   read only; the caller advances it after the call
+ *   k_new,v_new:[B,Hkv,D] or both NULL.  When given, norm(rope(k_new, p_b)) and v_new are written to cache
+ *                         row p_b (in place) and attended to; then p_b must be <= Tcap-1.
+ *   out:[B,Hq,D]
+ * Visible keys are j in [max(0, p_b - window), L_b) with L_b = p_b (+1 with a new key); window -1 = all.
+ * An empty visible set (p_b = 0 and no new key) gives a zero output row and no error.  A p_b outside the cache
+ * gives a zero output row and NC_ERR_DEVICE_BAD_INPUT in the device status word.  Requires Hq/Hkv <= 8.
+ *
+ * nc_attn_decode_ws takes a caller-owned device workspace of at least nc_attn_decode_workspace_bytes(...) bytes,
+ * 16-byte aligned.  It holds the split partial results and B*Hkv arrival counters.  The counters must be zero
+ * before the first call that uses the workspace (e.g. a zero-filled allocation); every call leaves them zero
+ * again.  Two calls that share a workspace must not overlap on the GPU.
+ * nc_attn_decode uses a workspace owned by the library (same growth and stream rules as nc_attn_fwd).
+ */
+size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, int window);
+
+nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                            const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
+                            int window, float rope_base, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                         const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap, int window,
+                         float rope_base, cudaStream_t stream);
+
+/* ---- status ------------------------------------------------------------------------------------------------------ */
+/* Static description of a status code (never NULL). */
+const char* nc_attn_status_string(nc_status s);
+
+/* Synchronizes `stream`, then returns the sticky device status of the current device (NC_OK when clean,
+ * NC_ERR_DEVICE_TIMEOUT or NC_ERR_DEVICE_BAD_INPUT otherwise; timeout wins) and, when `clear` is non-zero,
+ * resets it.  Returns NC_ERR_CUDA when the synchronization or the read fails. */
+nc_status nc_attn_get_device_status(cudaStream_t stream, int clear);
+
+/* Self-test of the bounded waits: launches one tiny kernel whose threads wait on a barrier that nothing ever
+ * completes, giving up after `limit_us` microseconds (1..2000000).  The kernel then returns normally and the
+ * device status reads NC_ERR_DEVICE_TIMEOUT.  Used by the tests to show that a stuck pipeline ends its kernel
+ * and leaves the context usable. */
+nc_status nc_attn_selftest_wait_timeout(int limit_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NC_ATTN_H */

@@ -1,0 +1,127 @@
+"""Host-side tests of the C ABI (no GPU needed, no kernel launched).
+
+* the shared library loads and exports every function ``include/nc_attn.h`` declares;
+* invalid arguments are rejected on the host with the documented status code before anything is launched;
+* workspace sizes and status strings.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nc_attn.h")
+
+
+@pytest.fixture(scope="module")
+def nc():
+    from transformer_attention_06_b300 import build
+    build.build()
+    from transformer_attention_06_b300 import nc_attn
+    return nc_attn
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nc_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("nc_attn_fwd", "nc_attn_fwd_ws", "nc_attn_decode", "nc_attn_decode_ws", "nc_attn_status_string",
+              "nc_attn_get_device_status", "nc_attn_qk_prologue"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(nc):
+    raw = ctypes.CDLL(nc.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+P = ctypes.c_void_p(0x10000)          # a non-null, 16-byte-aligned dummy address (never dereferenced)
+PM = ctypes.c_void_p(0x10008)         # misaligned
+
+
+def fwd(nc, q=P, k=P, v=P, out=P, B=1, T=256, Hq=4, Hkv=2, D=128, W=-1, base=1e5, ws=None, wsb=0):
+    return nc.lib.nc_attn_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, W, base, ws, wsb, None)
+
+
+def test_fwd_rejects_bad_arguments(nc):
+    E, U, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_UNSUPPORTED, nc.NC_ERR_WORKSPACE
+    assert fwd(nc, q=None) == E
+    assert fwd(nc, out=None) == E
+    assert fwd(nc, v=PM) == E
+    assert fwd(nc, B=0) == E
+    assert fwd(nc, T=0) == E
+    assert fwd(nc, Hq=3, Hkv=2) == E           # Hq % Hkv != 0
+    assert fwd(nc, W=-2) == E
+    assert fwd(nc, base=0.0) == E
+    assert fwd(nc, base=float("nan")) == E
+    assert fwd(nc, D=64) == U
+    assert fwd(nc, T=1 << 24) == U
+    assert fwd(nc, Hq=256, Hkv=1) == U          # group larger than one 128-row tile
+    assert fwd(nc) == WS                        # no workspace
+    need = nc.nc_attn_fwd_workspace_bytes(1, 256, 4, 2)
+    assert fwd(nc, ws=P, wsb=need - 1) == WS
+    assert fwd(nc, ws=PM, wsb=need) == WS
+
+
+def test_prologue_rejects_bad_arguments(nc):
+    f = nc.lib.nc_attn_qk_prologue
+    assert f(None, P, P, P, 1, 8, 2, 2, 128, 1e5, None) == nc.NC_ERR_INVALID_ARG
+    assert f(P, P, P, P, 1, 8, 2, 2, 96, 1e5, None) == nc.NC_ERR_UNSUPPORTED
+    assert f(P, P, P, P, 1, 8, 2, 2, 128, -1.0, None) == nc.NC_ERR_INVALID_ARG
+
+
+def dec(nc, q=P, kc=P, vc=P, lens=P, out=P, kn=None, vn=None, B=4, Hq=12, Hkv=4, D=128, Tcap=64, W=-1, base=1e5,
+        ws=None, wsb=0):
+    return nc.lib.nc_attn_decode_ws(q, kc, vc, lens, out, kn, vn, B, Hq, Hkv, D, Tcap, W, base, ws, wsb, None)
+
+
+def test_decode_rejects_bad_arguments(nc):
+    E, U, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_UNSUPPORTED, nc.NC_ERR_WORKSPACE
+    assert dec(nc, lens=None) == E
+    assert dec(nc, kc=None) == E
+    assert dec(nc, kn=P) == E                   # k_new without v_new
+    assert dec(nc, kn=P, vn=PM) == E
+    assert dec(nc, lens=ctypes.c_void_p(0x10002)) == E
+    assert dec(nc, Tcap=0) == E
+    assert dec(nc, Hq=10, Hkv=4) == E
+    assert dec(nc, W=-5) == E
+    assert dec(nc, base=float("inf")) == E
+    assert dec(nc, D=256) == U
+    assert dec(nc, Hq=36, Hkv=4) == U           # group of 9 > 8
+    assert dec(nc) == WS
+    need = nc.nc_attn_decode_workspace_bytes(4, 12, 4, 128, 64, -1)
+    assert dec(nc, ws=P, wsb=need - 1) == WS
+
+
+def test_workspace_sizes(nc):
+    # qn + kn in bf16 plus a small pad
+    assert nc.nc_attn_fwd_workspace_bytes(4, 2048, 6, 6) >= 2 * 4 * 2048 * 12 * 128
+    assert nc.nc_attn_fwd_workspace_bytes(0, 2048, 6, 6) == 0
+    # decode: counters + (m, l) + 128 floats per (b, kv head, chunk, group head); 17 chunks of 128 for window 2048
+    n = nc.nc_attn_decode_workspace_bytes(64, 12, 4, 128, 4097, 2048)
+    assert n >= 64 * 4 * 17 * 3 * 130 * 4
+    assert nc.nc_attn_decode_workspace_bytes(64, 12, 4, 128, 4097, 2048) > \
+        nc.nc_attn_decode_workspace_bytes(64, 12, 4, 128, 4097, 100)
+    assert nc.nc_attn_decode_workspace_bytes(64, 12, 4, 64, 4097, 2048) == 0
+
+
+def test_status_strings(nc):
+    for s in range(7):
+        assert nc.status_string(s).startswith("NC_")
+    assert "unknown" in nc.status_string(99)
+
+
+def test_binding_rejects_host_tensors(nc):
+    import torch
+    q = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        nc.nc_attn_fwd(q, q, q)
+    with pytest.raises(ValueError):
+        nc.nc_attn_decode(q[:, 0], q, q, torch.zeros(1, dtype=torch.int32))

@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded bf16 inputs.
+
+Tolerance: max-abs 2e-2 and mean-abs 2e-3 on bf16 outputs.  Small cases are compared element by element in full;
+the full-size workloads are compared on sampled rows that the oracle computes one by one, plus properties that hold
+at any size.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import ref
+from seeded_inputs import DECODE, DEPTH12, GQA, LONG, TINY, decode_inputs, fwd_inputs
+from tests.parity import assert_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transformer_attention_06_b300 import nc_attn
+    nc_attn.nc_attn_get_device_status(clear=True)
+    yield nc_attn
+    assert nc_attn.nc_attn_get_device_status(clear=True) == nc_attn.NC_OK
+
+
+def cuda(*ts):
+    return [t.cuda() if t is not None else None for t in ts]
+
+
+# ------------------------------------------------------------------------------------------------ prologue
+
+def test_prologue_matches_oracle_and_has_unit_rms(nc):
+    q, k, _ = fwd_inputs(2, 300, 6, 2, 128, seed=1)
+    qd, kd = cuda(q, k)
+    qn, kn = nc.nc_attn_qk_prologue(qd, kd)
+    torch.cuda.synchronize()
+    pos = np.broadcast_to(np.arange(300), (2, 300))
+    for got, x in ((qn, q), (kn, k)):
+        r = ref.qk_prologue(f64(x), pos)
+        g = f64(got)
+        # bf16 rounding of a value of size |r| costs at most 2^-9 |r|; allow 2^-8 |r| + 1e-3
+        assert np.all(np.abs(g - r) <= np.abs(r) * 2.0 ** -8 + 1e-3)
+        rms = np.sqrt(np.mean(g * g, axis=-1))
+        assert np.max(np.abs(rms - 1.0)) < 2.0 ** -8
+
+
+# ------------------------------------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("W", TINY.windows)
+def test_fwd_tiny_config(nc, W):
+    w = TINY
+    q, k, v = fwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=0)
+    out = nc.nc_attn_fwd(*cuda(q, k, v), window=W)
+    assert_close(out, ref.attn_fwd(f64(q), f64(k), f64(v), W), f"tiny W={W}")
+
+
+ODD = [  # (B, T, Hq, Hkv, W): T not a multiple of the tile, ragged tails, every group size the kernel packs
+    (1, 1, 1, 1, -1),
+    (2, 7, 2, 1, -1),
+    (1, 130, 3, 1, 5),
+    (2, 300, 8, 2, 127),
+    (1, 257, 12, 4, 0),
+    (1, 200, 6, 6, 1),
+    (1, 384, 16, 4, 200),
+    (1, 129, 5, 1, 64),
+    (2, 160, 4, 4, 128),
+    (1, 65, 32, 1, -1),
+    (1, 700, 2, 2, 300),
+]
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", ODD)
+def test_fwd_odd_shapes(nc, B, T, Hq, Hkv, W):
+    q, k, v = fwd_inputs(B, T, Hq, Hkv, 128, seed=T + Hq)
+    out = nc.nc_attn_fwd(*cuda(q, k, v), window=W)
+    assert_close(out, ref.attn_fwd(f64(q), f64(k), f64(v), W), f"B{B} T{T} Hq{Hq} Hkv{Hkv} W{W}")
+
+
+def sample_rows(B, T, Hq, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0, 0), (B - 1, T - 1, Hq - 1), (0, 1, Hq // 2), (B - 1, 127, 0), (0, 128, Hq - 1),
+            (0, T // 2, 1 % Hq), (B - 1, T - 2, Hq // 3)}
+    while len(rows) < n:
+        rows.add((int(rng.integers(B)), int(rng.integers(T)), int(rng.integers(Hq))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("wl", [DEPTH12, GQA, LONG], ids=lambda w: w.name)
+def test_fwd_full_size_sampled(nc, wl):
+    q, k, v = fwd_inputs(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D, seed=0)
+    qd, kd, vd = cuda(q, k, v)
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    G = wl.Hq // wl.Hkv
+    for W in sorted(set(wl.windows)):
+        out = nc.nc_attn_fwd(qd, kd, vd, window=W)
+        rows = sample_rows(wl.B, wl.T, wl.Hq, 48, seed=W)
+        exp = ref.attn_fwd_rows(qf, kf, vf, W, rows)
+        got = torch.stack([out[b, i, h] for (b, i, h) in rows])
+        assert_close(got, exp, f"{wl.name} W={W} sampled")
+        # position 0 sees only itself: the output is v_0 of the group's kv head, at any size
+        o0 = f64(out[:, 0])
+        v0 = f64(v[:, 0])
+        for h in range(wl.Hq):
+            assert np.max(np.abs(o0[:, h] - v0[:, h // G])) < 1e-6
+        assert torch.isfinite(out).all()
+
+
+def test_window_at_least_T_minus_1_equals_full_causal(nc):
+    q, k, v = cuda(*fwd_inputs(2, 515, 6, 2, 128, seed=5))
+    full = nc.nc_attn_fwd(q, k, v, window=-1).clone()
+    for W in (514, 515, 100000):
+        assert torch.equal(nc.nc_attn_fwd(q, k, v, window=W), full)
+
+
+def test_gqa_equals_mha_with_repeated_kv(nc):
+    q, k, v = fwd_inputs(1, 333, 8, 2, 128, seed=6)
+    qd, kd, vd = cuda(q, k, v)
+    a = nc.nc_attn_fwd(qd, kd, vd, window=50).clone()
+    b = nc.nc_attn_fwd(qd, kd.repeat_interleave(4, dim=2).contiguous(), vd.repeat_interleave(4, dim=2).contiguous(),
+                       window=50)
+    assert_close(a, f64(b), "GQA vs repeated-KV MHA (GPU vs GPU)")
+
+
+@pytest.mark.parametrize("W", [-1, 40])
+def test_causality_and_band_on_gpu(nc, W):
+    q, k, v = fwd_inputs(1, 400, 4, 2, 128, seed=7)
+    qd, kd, vd = cuda(q, k, v)
+    base = nc.nc_attn_fwd(qd, kd, vd, window=W).clone()
+    i = 200
+    k2, v2 = kd.clone(), vd.clone()
+    k2[:, i + 1:] *= -3
+    v2[:, i + 1:] += 5
+    if W >= 0:
+        k2[:, :i - W] *= 2
+        v2[:, :i - W] -= 7
+    out = nc.nc_attn_fwd(qd, k2, v2, window=W)
+    assert torch.equal(out[:, i], base[:, i])
+
+
+# ------------------------------------------------------------------------------------------------ decode
+
+def decode_case(nc, B, Hq, Hkv, Tcap, lens, W, with_new, seed):
+    d = decode_inputs(B, Hq, Hkv, 128, Tcap, 1, 2, seed=seed, with_new=with_new)
+    lens = torch.tensor(lens, dtype=torch.int32)
+    kc, vc = d["kcache"].clone(), d["vcache"].clone()
+    q, kn, vn = d["q"], d["k_new"], d["v_new"]
+    exp, kn_ref = ref.attn_decode(f64(q), f64(kc), f64(vc), lens.numpy(), W,
+                                  f64(kn) if with_new else None, f64(vn) if with_new else None)
+    kcd, vcd = cuda(kc, vc)
+    out = nc.nc_attn_decode(*cuda(q), kcd, vcd, lens.cuda(), k_new=kn.cuda() if with_new else None,
+                            v_new=vn.cuda() if with_new else None, window=W)
+    torch.cuda.synchronize()
+    return out, exp, kcd, vcd, kn_ref, d, lens
+
+
+@pytest.mark.parametrize("W", [-1, 0, 5, 128, 2048])
+@pytest.mark.parametrize("with_new", [False, True])
+def test_decode_small(nc, W, with_new):
+    lens = [0, 1, 127, 128, 129, 255, 256, 298]
+    out, exp, kcd, vcd, kn_ref, d, lens_t = decode_case(nc, len(lens), 12, 4, 300, lens, W, with_new, seed=3)
+    assert_close(out, exp, f"decode W={W} new={with_new}")
+    if with_new:
+        for b, p in enumerate(lens):
+            g = f64(kcd[b, p])
+            assert np.all(np.abs(g - kn_ref[b]) <= np.abs(kn_ref[b]) * 2.0 ** -8 + 1e-3)
+            assert torch.equal(vcd[b, p].cpu(), d["v_new"][b])
+    else:
+        assert torch.count_nonzero(out[0]) == 0       # empty visible set
+
+
+@pytest.mark.parametrize("G", [1, 2, 8])
+def test_decode_group_sizes(nc, G):
+    lens = [3, 500, 1000]
+    out, exp, *_ = decode_case(nc, 3, 2 * G, 2, 1024, lens, 300, True, seed=G)
+    assert_close(out, exp, f"decode G={G}")
+
+
+def test_decode_full_config(nc):
+    w = DECODE
+    for with_new in (False, True):
+        d = decode_inputs(w.B, w.Hq, w.Hkv, w.D, w.Tcap, w.len_lo, w.len_hi, seed=0, with_new=with_new)
+        lens = d["cache_lens"]
+        exp, _ = ref.attn_decode(f64(d["q"]), d["kcache"].float().numpy(), d["vcache"].float().numpy(),
+                                 lens.numpy(), w.window, f64(d["k_new"]) if with_new else None,
+                                 f64(d["v_new"]) if with_new else None)
+        kc, vc = cuda(d["kcache"], d["vcache"])
+        out = nc.nc_attn_decode(d["q"].cuda(), kc, vc, lens.cuda(),
+                                k_new=d["k_new"].cuda() if with_new else None,
+                                v_new=d["v_new"].cuda() if with_new else None, window=w.window)
+        assert_close(out, exp, f"decode full config new={with_new}")
+        # a second call on the same workspace gives the same result (the counters were left at zero)
+        out2 = nc.nc_attn_decode(d["q"].cuda(), kc, vc, lens.cuda(),
+                                 k_new=d["k_new"].cuda() if with_new else None,
+                                 v_new=d["v_new"].cuda() if with_new else None, window=w.window)
+        assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("W", [-1, 33])
+def test_decode_equals_prefill_row_on_gpu(nc, W):
+    """Cache-vs-full self-consistency between the two GPU kernels: decode of token p against a cache holding the
+    prologue's kn[0:p] and v[0:p] (plus k[p], v[p] as the new key/value) equals prefill row p."""
+    B, T, Hq, Hkv = 2, 300, 6, 2
+    q, k, v = cuda(*fwd_inputs(B, T, Hq, Hkv, 128, seed=9))
+    full = nc.nc_attn_fwd(q, k, v, window=W)
+    _, kn = nc.nc_attn_qk_prologue(q, k)
+    for p in (0, 1, 150, 299):
+        kc = torch.zeros(B, T, Hkv, 128, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        kc[:, :p] = kn[:, :p]
+        vc[:, :p] = v[:, :p]
+        lens = torch.full((B,), p, dtype=torch.int32, device="cuda")
+        out = nc.nc_attn_decode(q[:, p].contiguous(), kc, vc, lens, k_new=k[:, p].contiguous(),
+                                v_new=v[:, p].contiguous(), window=W)
+        assert_close(out, f64(full[:, p]), f"decode vs prefill row p={p} W={W}")
+        assert torch.equal(kc[:, p], kn[:, p])    # the new key is written exactly as the prologue computes it
+
+
+def test_decode_bad_cache_length_sets_status_and_zero_row(nc):
+    d = decode_inputs(3, 4, 2, 128, 64, 1, 60, seed=4, with_new=True)
+    lens = torch.tensor([10, 64, -1], dtype=torch.int32)   # 64 = Tcap: no room for the new key
+    kc, vc = cuda(d["kcache"], d["vcache"])
+    out = nc.nc_attn_decode(d["q"].cuda(), kc, vc, lens.cuda(), k_new=d["k_new"].cuda(), v_new=d["v_new"].cuda(),
+                            window=-1)
+    assert nc.nc_attn_get_device_status(clear=True) == nc.NC_ERR_DEVICE_BAD_INPUT
+    assert torch.count_nonzero(out[1:]) == 0
+    exp, _ = ref.attn_decode(f64(d["q"][:1]), f64(d["kcache"][:1]), f64(d["vcache"][:1]), lens[:1].numpy(), -1,
+                             f64(d["k_new"][:1]), f64(d["v_new"][:1]))
+    assert_close(out[:1], exp, "valid row next to invalid ones")
+    assert nc.nc_attn_get_device_status(clear=True) == nc.NC_OK
+
+
+# ------------------------------------------------------------------------------------------------ bounded waits
+
+def test_bounded_wait_times_out_and_context_survives(nc):
+    nc.nc_attn_selftest_wait_timeout(2000)       # 2 ms limit on a barrier nothing completes
+    assert nc.nc_attn_get_device_status(clear=True) == nc.NC_ERR_DEVICE_TIMEOUT
+    assert nc.nc_attn_get_device_status(clear=True) == nc.NC_OK
+    q, k, v = fwd_inputs(1, 64, 2, 1, 128, seed=1)
+    out = nc.nc_attn_fwd(*cuda(q, k, v))
+    assert_close(out, ref.attn_fwd(f64(q), f64(k), f64(v), -1), "after the timeout self-test")

@@ -1,0 +1,395 @@
+// C-ABI entry points of the attention library: host-side validation, TMA descriptor encoding, launch
+// configuration and workspace layout.  One translation unit holds every kernel, so that the device status word is
+// a single symbol without relocatable device code.
+//
+// Nothing here falls back to the CPU or to another implementation: an unsupported request returns an error code.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "nc_attn.h"
+
+#include "common.cuh"
+#include "prologue.cuh"
+#include "attn_fwd.cuh"
+#include "attn_decode.cuh"
+
+namespace {
+
+using nc::RopeTable;
+
+constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per bounded wait
+
+// ---------------------------------------------------------------------------------------------------------------
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// A 4-D bf16 view [d3][d2][d1][d0] (d0 innermost, contiguous), 128-byte swizzle, zero fill out of bounds.
+bool make_map_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+                 uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {d0, d1, d2, d3};
+  const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  const cuuint32_t box[4] = {b0, b1, b2, b3};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------------------------------------------
+RopeTable rope_table(float base) {
+  // theta_i = base^(-2i/D) for D = 128, in fp64, split into an fp32 value and its fp32 residual.
+  RopeTable t;
+  for (int i = 0; i < 64; ++i) {
+    const double th = std::pow(static_cast<double>(base), -2.0 * i / 128.0);
+    t.hi[i] = static_cast<float>(th);
+    t.lo[i] = static_cast<float>(th - static_cast<double>(t.hi[i]));
+  }
+  return t;
+}
+
+float scale_log2_for_d128() { return static_cast<float>(1.4426950408889634 / std::sqrt(128.0)); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool rope_base_ok(float base) { return std::isfinite(base) && base > 0.f; }
+
+// Checks shared by the forward and the prologue.  Returns NC_OK or the error to report.
+nc_status check_fwd_shapes(int B, int T, int Hq, int Hkv, int D) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1) return NC_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return NC_ERR_INVALID_ARG;
+  if (D != 128) return NC_ERR_UNSUPPORTED;
+  if (T >= (1 << 24)) return NC_ERR_UNSUPPORTED;  // positions must be exact in fp32
+  const long double elems = static_cast<long double>(B) * T * Hq * D;
+  if (elems > 9.0e15L) return NC_ERR_INVALID_ARG;
+  return NC_OK;
+}
+
+template <typename F>
+void set_smem_attr_once(F* kernel, int bytes, int slot) {
+  static bool done[16][8] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 16) dev = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev][slot]) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    done[dev][slot] = true;
+  }
+}
+
+nc_status launch_status() { return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA; }
+
+nc_status launch_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
+                          const RopeTable& tab, cudaStream_t stream) {
+  const int BT = B * T;
+  const int blocks = (BT + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
+  nc::qk_prologue_kernel<<<blocks, nc::kPrologueThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(qn),
+      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab);
+  return launch_status();
+}
+
+// ---- library-held workspaces for the entry points without a workspace argument -------------------------------
+struct HeldBuffer {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+std::mutex g_ws_mu;
+HeldBuffer g_fwd_ws[16];
+HeldBuffer g_dec_ws[16];
+
+// Returns a buffer of at least `bytes` for the current device, grown in stream order; `zero` clears a new buffer.
+void* held_workspace(HeldBuffer* table, size_t bytes, bool zero, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return nullptr;
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  HeldBuffer& hb = table[dev];
+  if (hb.bytes < bytes) {
+    if (hb.ptr != nullptr) cudaFreeAsync(hb.ptr, stream);
+    hb.ptr = nullptr;
+    hb.bytes = 0;
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) return nullptr;
+    if (zero && cudaMemsetAsync(p, 0, bytes, stream) != cudaSuccess) return nullptr;
+    hb.ptr = p;
+    hb.bytes = bytes;
+  }
+  return hb.ptr;
+}
+
+// ---- decode workspace layout ------------------------------------------------------------------------------------
+struct DecodeLayout {
+  int n_chunks;
+  size_t off_cnt, off_ml, off_o, total;
+};
+
+DecodeLayout decode_layout(int B, int Hq, int Hkv, int Tcap, int window) {
+  DecodeLayout L;
+  const int G = Hq / Hkv;
+  const long long span = (window < 0) ? Tcap : std::min<long long>(static_cast<long long>(window) + 1, Tcap);
+  L.n_chunks = static_cast<int>((span + nc::dec::kC - 1) / nc::dec::kC);
+  if (L.n_chunks < 1) L.n_chunks = 1;
+  const size_t slots = static_cast<size_t>(B) * Hkv * L.n_chunks * G;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  L.off_cnt = 0;
+  L.off_ml = up(static_cast<size_t>(B) * Hkv * sizeof(unsigned));
+  L.off_o = L.off_ml + up(slots * 2 * sizeof(float));
+  L.total = L.off_o + up(slots * 128 * sizeof(float));
+  return L;
+}
+
+nc_status check_decode_args(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
+                            const void* out, const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D,
+                            int Tcap, int window, float rope_base) {
+  if (q == nullptr || kcache == nullptr || vcache == nullptr || cache_lens == nullptr || out == nullptr)
+    return NC_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return NC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out)) return NC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID_ARG;
+  if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return NC_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || Tcap < 1) return NC_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return NC_ERR_INVALID_ARG;
+  if (window < -1) return NC_ERR_INVALID_ARG;
+  if (!rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
+  if (D != 128) return NC_ERR_UNSUPPORTED;
+  if (Hq / Hkv > nc::dec::kMaxG) return NC_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535 || Tcap >= (1 << 24)) return NC_ERR_UNSUPPORTED;
+  return NC_OK;
+}
+
+template <int G>
+void launch_decode_g(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv, const RopeTable& tab,
+                     const nc::dec::Params& prm, cudaStream_t stream) {
+  set_smem_attr_once(nc::dec::attn_decode_kernel<G>, nc::dec::kSmemBytes, 1 + G);
+  nc::dec::attn_decode_kernel<G><<<grid, nc::dec::kThreads, nc::dec::kSmemBytes, stream>>>(mk, mv, tab, prm);
+}
+
+}  // namespace
+
+// =================================================================================================================
+extern "C" {
+
+size_t nc_attn_fwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
+  if (check_fwd_shapes(B, T, Hq, Hkv, D) != NC_OK && !(D > 0 && D != 128)) return 0;
+  return 2ull * static_cast<size_t>(B) * T * (Hq + Hkv) * D + 256;
+}
+
+nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
+                              int D, float rope_base, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || qn == nullptr || kn == nullptr) return NC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(qn) || !aligned16(kn)) return NC_ERR_INVALID_ARG;
+  if (!rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
+  const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
+  if (st != NC_OK) return st;
+  return launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), stream);
+}
+
+nc_status nc_attn_fwd_ws(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                         int D, int window, float rope_base, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  return nc_attn_fwd_ws_events(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, workspace, workspace_bytes,
+                               nullptr, nullptr, nullptr, stream);
+}
+
+nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,
+                                int Hkv, int D, int window, float rope_base, void* workspace,
+                                size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin,
+                                cudaEvent_t k2_end, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return NC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NC_ERR_INVALID_ARG;
+  if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
+  nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
+  if (st != NC_OK) return st;
+  const int G = Hq / Hkv;
+  if (G > 128) return NC_ERR_UNSUPPORTED;
+  const int P = 128 / G;
+  const int n_qtiles = (T + P - 1) / P;
+  if (n_qtiles > 65535 || static_cast<long long>(B) * Hkv > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
+  const size_t need = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return NC_ERR_WORKSPACE;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qn = ws;
+  void* kn = ws + 2ull * static_cast<size_t>(B) * T * Hq * D;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map_4d(&mq, qn, 128, Hq, T, B, 64, G, P, 1) || !make_map_4d(&mk, kn, 128, Hkv, T, B, 64, 1, 128, 1) ||
+      !make_map_4d(&mv, v, 128, Hkv, T, B, 64, 1, 128, 1))
+    return NC_ERR_CUDA;
+
+  if (k1_begin != nullptr && cudaEventRecord(k1_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
+  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), stream);
+  if (st != NC_OK) return st;
+  if (k2_begin != nullptr && cudaEventRecord(k2_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
+
+  nc::fwd::Params prm;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.B = B;
+  prm.T = T;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.G = G;
+  prm.P = P;
+  prm.n_qtiles = n_qtiles;
+  prm.window = window;
+  prm.scale_log2 = scale_log2_for_d128();
+  prm.wait_limit_ns = kWaitLimitNs;
+  set_smem_attr_once(nc::fwd::attn_fwd_kernel, nc::fwd::kSmemBytes, 0);
+  dim3 grid(B * Hkv, n_qtiles);
+  nc::fwd::attn_fwd_kernel<<<grid, nc::fwd::kThreads, nc::fwd::kSmemBytes, stream>>>(mq, mk, mv, prm);
+  st = launch_status();
+  if (st == NC_OK && k2_end != nullptr && cudaEventRecord(k2_end, stream) != cudaSuccess) return NC_ERR_CUDA;
+  return st;
+}
+
+nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv, int D,
+                      int window, float rope_base, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return NC_ERR_INVALID_ARG;
+  const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
+  if (st != NC_OK) return st;
+  const size_t need = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
+  void* ws = held_workspace(g_fwd_ws, need, false, stream);
+  if (ws == nullptr) return NC_ERR_CUDA;
+  return nc_attn_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, ws, need, stream);
+}
+
+size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, int window) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || D != 128 || Tcap < 1 || Hq % Hkv != 0 || window < -1) return 0;
+  return decode_layout(B, Hq, Hkv, Tcap, window).total;
+}
+
+nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                            const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
+                            int window, float rope_base, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  const nc_status st =
+      check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
+  if (st != NC_OK) return st;
+  const DecodeLayout L = decode_layout(B, Hq, Hkv, Tcap, window);
+  if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return NC_ERR_WORKSPACE;
+
+  CUtensorMap mk, mv;
+  if (!make_map_4d(&mk, kcache, 128, Hkv, Tcap, B, 64, 1, nc::dec::kC, 1) ||
+      !make_map_4d(&mv, vcache, 128, Hkv, Tcap, B, 64, 1, nc::dec::kC, 1))
+    return NC_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  nc::dec::Params prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.kcache = static_cast<__nv_bfloat16*>(kcache);
+  prm.vcache = static_cast<__nv_bfloat16*>(vcache);
+  prm.cache_lens = cache_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  prm.ws_cnt = reinterpret_cast<unsigned*>(ws + L.off_cnt);
+  prm.ws_ml = reinterpret_cast<float*>(ws + L.off_ml);
+  prm.ws_o = reinterpret_cast<float*>(ws + L.off_o);
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Tcap = Tcap;
+  prm.window = window;
+  prm.n_chunks = L.n_chunks;
+  prm.scale_log2 = scale_log2_for_d128();
+  prm.wait_limit_ns = kWaitLimitNs;
+  const RopeTable tab = rope_table(rope_base);
+  const dim3 grid(L.n_chunks, Hkv, B);
+  switch (Hq / Hkv) {
+    case 1: launch_decode_g<1>(grid, mk, mv, tab, prm, stream); break;
+    case 2: launch_decode_g<2>(grid, mk, mv, tab, prm, stream); break;
+    case 3: launch_decode_g<3>(grid, mk, mv, tab, prm, stream); break;
+    case 4: launch_decode_g<4>(grid, mk, mv, tab, prm, stream); break;
+    case 5: launch_decode_g<5>(grid, mk, mv, tab, prm, stream); break;
+    case 6: launch_decode_g<6>(grid, mk, mv, tab, prm, stream); break;
+    case 7: launch_decode_g<7>(grid, mk, mv, tab, prm, stream); break;
+    case 8: launch_decode_g<8>(grid, mk, mv, tab, prm, stream); break;
+    default: return NC_ERR_UNSUPPORTED;
+  }
+  return launch_status();
+}
+
+nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                         const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap, int window,
+                         float rope_base, cudaStream_t stream) {
+  const nc_status st =
+      check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
+  if (st != NC_OK) return st;
+  const size_t need = decode_layout(B, Hq, Hkv, Tcap, window).total;
+  void* ws = held_workspace(g_dec_ws, need, true, stream);
+  if (ws == nullptr) return NC_ERR_CUDA;
+  return nc_attn_decode_ws(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window,
+                           rope_base, ws, need, stream);
+}
+
+const char* nc_attn_status_string(nc_status s) {
+  switch (s) {
+    case NC_OK: return "NC_OK: success";
+    case NC_ERR_INVALID_ARG: return "NC_ERR_INVALID_ARG: null or misaligned pointer, bad size, window or rope base";
+    case NC_ERR_UNSUPPORTED: return "NC_ERR_UNSUPPORTED: valid request outside what this library implements";
+    case NC_ERR_CUDA: return "NC_ERR_CUDA: a CUDA call or kernel launch failed";
+    case NC_ERR_DEVICE_TIMEOUT: return "NC_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
+    case NC_ERR_DEVICE_BAD_INPUT: return "NC_ERR_DEVICE_BAD_INPUT: a kernel found a cache length outside the cache";
+    case NC_ERR_WORKSPACE: return "NC_ERR_WORKSPACE: workspace missing, misaligned or too small";
+  }
+  return "unknown nc_status";
+}
+
+nc_status nc_attn_get_device_status(cudaStream_t stream, int clear) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return NC_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, nc::g_status, sizeof(v)) != cudaSuccess) return NC_ERR_CUDA;
+  if (clear && v != 0) {
+    const unsigned z = 0;
+    if (cudaMemcpyToSymbol(nc::g_status, &z, sizeof(z)) != cudaSuccess) return NC_ERR_CUDA;
+  }
+  if (v & nc::NC_DEV_TIMEOUT) return NC_ERR_DEVICE_TIMEOUT;
+  if (v & nc::NC_DEV_BAD_CACHE_LEN) return NC_ERR_DEVICE_BAD_INPUT;
+  return NC_OK;
+}
+
+}  // extern "C"
+
+namespace nc {
+// One warp waits on a barrier that nothing completes; the bounded wait gives up and raises NC_DEV_TIMEOUT.
+__global__ void selftest_wait_timeout_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, limit_ns, &abort_flag);
+}
+}  // namespace nc
+
+extern "C" nc_status nc_attn_selftest_wait_timeout(int limit_us, cudaStream_t stream) {
+  if (limit_us < 1 || limit_us > 2000000) return NC_ERR_INVALID_ARG;
+  nc::selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(limit_us) * 1000ull);
+  return launch_status();
+}

@@ -1,0 +1,99 @@
+// K1: fused RoPE + QK-norm prologue of the prefill forward.
+//
+// For every token (b, t) and every q head and k head: rotate the half-split pairs (i, i + 64) by t * theta_i, then
+// divide the vector by sqrt(mean(y^2) + eps).  ("nanochat Admin & Developer Guide", section 3: RoPE base 100000,
+// QK-norm, RMSNorm without parameters; "nanochat (Fucina port)", "Architecture": half-split RoPE.)
+//
+// Memory-bound: it reads q and k once and writes qn and kn once (2 * 2 * B*T*(Hq+Hkv)*128 bytes).  Mapping: an
+// 8-lane group per token; lane kq of the group owns pairs [8kq, 8kq+8), i.e. two 16-byte slices of every head
+// vector of the token, so the cos/sin of the token are computed once and reused across all Hq + Hkv heads.  The
+// sum of squares is reduced across the group with three xor-shuffles.
+#pragma once
+
+#include "common.cuh"
+
+namespace nc {
+
+// Rotates the 8 pairs held in (lo, hi) -- elements [8kq, 8kq+8) and [64+8kq, 64+8kq+8) of a 128-wide head
+// vector -- and normalises by the RMS of the whole vector (reduced over the 8-lane group `gmask`).
+__device__ __forceinline__ void rope_norm_slices(const uint4& lo, const uint4& hi, const float (&c)[8],
+                                                 const float (&s)[8], unsigned gmask, float (&y1)[8],
+                                                 float (&y2)[8]) {
+  const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w};
+  const uint32_t b[4] = {hi.x, hi.y, hi.z, hi.w};
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x1 = (i & 1) ? bf16_hi(a[i >> 1]) : bf16_lo(a[i >> 1]);
+    const float x2 = (i & 1) ? bf16_hi(b[i >> 1]) : bf16_lo(b[i >> 1]);
+    y1[i] = fmaf(x1, c[i], x2 * s[i]);
+    y2[i] = fmaf(x2, c[i], -(x1 * s[i]));
+    ss = fmaf(y1[i], y1[i], ss);
+    ss = fmaf(y2[i], y2[i], ss);
+  }
+  ss += __shfl_xor_sync(gmask, ss, 1);
+  ss += __shfl_xor_sync(gmask, ss, 2);
+  ss += __shfl_xor_sync(gmask, ss, 4);
+  const float inv = rsqrtf(ss * (1.0f / 128.0f) + kRmsEps);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    y1[i] *= inv;
+    y2[i] *= inv;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&y)[8]) {
+  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                    pack_bf16x2(y[6], y[7]));
+}
+
+// Processes `H` consecutive head vectors of one token (src/dst point at head 0), four at a time so that eight
+// 16-byte loads per lane are in flight before any arithmetic.
+__device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                                int H, int kq, const float (&c)[8], const float (&s)[8],
+                                                unsigned gmask) {
+  const uint4* in = reinterpret_cast<const uint4*>(src);
+  uint4* out = reinterpret_cast<uint4*>(dst);
+  for (int h0 = 0; h0 < H; h0 += 4) {
+    uint4 lo[4], hi[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (h0 + u < H) {
+        lo[u] = __ldg(in + (h0 + u) * 16 + kq);
+        hi[u] = __ldg(in + (h0 + u) * 16 + 8 + kq);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (h0 + u < H) {
+        float y1[8], y2[8];
+        rope_norm_slices(lo[u], hi[u], c, s, gmask, y1, y2);
+        out[(h0 + u) * 16 + kq] = pack8_bf16(y1);
+        out[(h0 + u) * 16 + 8 + kq] = pack8_bf16(y2);
+      }
+    }
+  }
+}
+
+constexpr int kPrologueThreads = 256;
+constexpr int kPrologueTokensPerBlock = kPrologueThreads / 8;
+
+__global__ void __launch_bounds__(kPrologueThreads)
+    qk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                       __nv_bfloat16* __restrict__ qn, __nv_bfloat16* __restrict__ kn, int BT, int T, int Hq,
+                       int Hkv, const __grid_constant__ RopeTable tab) {
+  const int tok = blockIdx.x * kPrologueTokensPerBlock + (threadIdx.x >> 3);
+  const int kq = threadIdx.x & 7;
+  if (tok >= BT) return;  // whole 8-lane groups leave together
+  const unsigned gmask = 0xFFu << ((threadIdx.x & 31) & ~7);
+  const float pos = static_cast<float>(tok % T);
+  float c[8], s[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rope_cos_sin(pos, tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
+  rope_norm_heads(q + static_cast<size_t>(tok) * Hq * 128, qn + static_cast<size_t>(tok) * Hq * 128, Hq, kq, c, s,
+                  gmask);
+  rope_norm_heads(k + static_cast<size_t>(tok) * Hkv * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq, c,
+                  s, gmask);
+}
+
+}  // namespace nc

@@ -1,0 +1,205 @@
+"""Python binding of the C-ABI library ``libnc_attn.so`` (argument marshalling only).
+
+Every function here checks the torch tensors it is given (device, dtype, contiguity, shapes), passes their device
+pointers and the current CUDA stream to the library entry point of the same name, and raises ``NcAttnError`` on a
+non-zero status.  All arithmetic runs in the library's CUDA kernels; there is no other implementation and no CPU
+fallback: if the shared library is missing, importing this module fails.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnc_attn.so")
+
+ROPE_BASE = 100000.0
+
+NC_OK = 0
+NC_ERR_INVALID_ARG = 1
+NC_ERR_UNSUPPORTED = 2
+NC_ERR_CUDA = 3
+NC_ERR_DEVICE_TIMEOUT = 4
+NC_ERR_DEVICE_BAD_INPUT = 5
+NC_ERR_WORKSPACE = 6
+
+
+class NcAttnError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m transformer_attention_06_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sigs = {
+        "nc_attn_fwd_workspace_bytes": (sz, [i, i, i, i, i]),
+        "nc_attn_fwd_ws": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp]),
+        "nc_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
+        "nc_attn_fwd_ws_events": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp, vp, vp]),
+        "nc_attn_qk_prologue": (i, [vp, vp, vp, vp, i, i, i, i, i, f, vp]),
+        "nc_attn_decode_workspace_bytes": (sz, [i, i, i, i, i, i]),
+        "nc_attn_decode_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp]),
+        "nc_attn_decode": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
+        "nc_attn_status_string": (ctypes.c_char_p, [i]),
+        "nc_attn_get_device_status": (i, [vp, i]),
+        "nc_attn_selftest_wait_timeout": (i, [i, vp]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status):
+    return lib.nc_attn_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != NC_OK:
+        raise NcAttnError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, name, ndim, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# Workspaces cached per (device, kind); the decode one starts zero-filled and every call leaves its counters zero.
+_ws_cache = {}
+
+
+def _workspace(kind, nbytes, device, zero):
+    key = (kind, device.index if device.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = (torch.zeros if zero else torch.empty)(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D=128):
+    return int(lib.nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D))
+
+
+def nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window):
+    return int(lib.nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window))
+
+
+def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=None, stream=None, events=None):
+    """Prefill / training forward.  q [B,T,Hq,D], k and v [B,T,Hkv,D] (bf16, CUDA, contiguous) -> out [B,T,Hq,D].
+
+    ``events``: optional (k1_begin, k2_begin, k2_end) torch.cuda.Event objects (any may be None), recorded on the
+    stream around the prologue kernel and the attention kernel.
+    """
+    _need(q, "q", 4)
+    _need(k, "k", 4)
+    _need(v, "v", 4)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, T, Hkv, D) or tuple(v.shape) != (B, T, Hkv, D):
+        raise ValueError(f"k/v shapes {tuple(k.shape)}/{tuple(v.shape)} do not match q {tuple(q.shape)}")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", 4)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have the shape of q")
+    nbytes = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D)
+    if workspace is None:
+        workspace = _workspace("fwd", nbytes, q.device, zero=False)
+    ev = [ctypes.c_void_p(e.cuda_event) if e is not None else None for e in (events or (None, None, None))]
+    st = lib.nc_attn_fwd_ws_events(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, D, int(window),
+                                   float(rope_base), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   ev[0], ev[1], ev[2], _stream(stream))
+    _check(st, "nc_attn_fwd")
+    return out
+
+
+def nc_attn_qk_prologue(q, k, qn=None, kn=None, rope_base=ROPE_BASE, stream=None):
+    """RoPE + weightless RMSNorm of q [B,T,Hq,D] and k [B,T,Hkv,D] at positions 0..T-1 -> (qn, kn), bf16."""
+    _need(q, "q", 4)
+    _need(k, "k", 4)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, T, Hkv, D):
+        raise ValueError("k shape does not match q")
+    qn = torch.empty_like(q) if qn is None else qn
+    kn = torch.empty_like(k) if kn is None else kn
+    _need(qn, "qn", 4)
+    _need(kn, "kn", 4)
+    st = lib.nc_attn_qk_prologue(_ptr(q), _ptr(k), _ptr(qn), _ptr(kn), B, T, Hq, Hkv, D, float(rope_base),
+                                 _stream(stream))
+    _check(st, "nc_attn_qk_prologue")
+    return qn, kn
+
+
+def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=None, window=-1,
+                   rope_base=ROPE_BASE, workspace=None, stream=None):
+    """Single-token decode.  q [B,Hq,D]; caches [B,Tcap,Hkv,D]; cache_lens int32 [B] (device) -> out [B,Hq,D].
+
+    With k_new / v_new [B,Hkv,D], the new key (roped + normed at cache_lens[b]) and value are written into the caches
+    at row cache_lens[b] and attended to.  cache_lens is not modified.
+    """
+    _need(q, "q", 3)
+    _need(kcache, "kcache", 4)
+    _need(vcache, "vcache", 4)
+    _need(cache_lens, "cache_lens", 1, dtype=torch.int32)
+    B, Hq, D = q.shape
+    _, Tcap, Hkv, _ = kcache.shape
+    if tuple(kcache.shape) != (B, Tcap, Hkv, D) or tuple(vcache.shape) != (B, Tcap, Hkv, D):
+        raise ValueError("cache shapes do not match q")
+    if cache_lens.shape[0] != B:
+        raise ValueError("cache_lens must have B entries")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        _need(k_new, "k_new", 3)
+        _need(v_new, "v_new", 3)
+        if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+            raise ValueError("k_new / v_new must be [B, Hkv, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", 3)
+    nbytes = nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, int(window))
+    if workspace is None:
+        workspace = _workspace("decode", nbytes, q.device, zero=True)
+    st = lib.nc_attn_decode_ws(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
+                               _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nc_attn_decode")
+    return out
+
+
+def nc_attn_get_device_status(clear=True, stream=None):
+    """Synchronizes the stream and returns the sticky device status code (NC_OK when clean)."""
+    return int(lib.nc_attn_get_device_status(_stream(stream), 1 if clear else 0))
+
+
+def nc_attn_selftest_wait_timeout(limit_us, stream=None):
+    _check(lib.nc_attn_selftest_wait_timeout(int(limit_us), _stream(stream)), "nc_attn_selftest_wait_timeout")
