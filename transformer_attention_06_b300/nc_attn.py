@@ -74,6 +74,16 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _event_handle(e, stream):
+    """Raw cudaEvent_t of a torch.cuda.Event.  torch creates the CUDA event on its first record, so an event that was
+    never recorded is recorded once here (the library records it again at the right place)."""
+    if e is None:
+        return None
+    if e.cuda_event == 0:
+        e.record(stream if stream is not None else torch.cuda.current_stream())
+    return ctypes.c_void_p(e.cuda_event)
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
@@ -133,7 +143,7 @@ def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=Non
     nbytes = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D)
     if workspace is None:
         workspace = _workspace("fwd", nbytes, q.device, zero=False)
-    ev = [ctypes.c_void_p(e.cuda_event) if e is not None else None for e in (events or (None, None, None))]
+    ev = [_event_handle(e, stream) for e in (events or (None, None, None))]
     st = lib.nc_attn_fwd_ws_events(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, D, int(window),
                                    float(rope_base), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    ev[0], ev[1], ev[2], _stream(stream))
