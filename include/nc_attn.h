@@ -97,9 +97,11 @@ nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, 
  * gives a zero output row and NC_ERR_DEVICE_BAD_INPUT in the device status word.  Requires Hq/Hkv <= 8.
  *
  * nc_attn_decode_ws takes a caller-owned device workspace of at least nc_attn_decode_workspace_bytes(...) bytes,
- * 16-byte aligned.  It holds the split partial results and B*Hkv arrival counters.  The counters must be zero
- * before the first call that uses the workspace (e.g. a zero-filled allocation); every call leaves them zero
- * again.  Two calls that share a workspace must not overlap on the GPU.
+ * 16-byte aligned.  It holds B*Hkv arrival counters at its start, then the split partial results.  The counters
+ * must be zero when a call starts: zero the workspace before its first use (e.g. a zero-filled allocation) and
+ * again before any call whose B*Hkv differs from that of the previous call on the same workspace (that call's
+ * partials may lie where the new counters go).  A call leaves its own counters zero, so calls with the same B and
+ * Hkv can reuse the workspace as is.  Two calls that share a workspace must not overlap on the GPU.
  * nc_attn_decode uses a workspace owned by the library (same growth and stream rules as nc_attn_fwd).
  */
 size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, int window);

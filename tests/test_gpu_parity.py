@@ -218,6 +218,37 @@ def test_decode_equals_prefill_row_on_gpu(nc, W):
         assert torch.equal(kc[:, p], kn[:, p])    # the new key is written exactly as the prologue computes it
 
 
+def test_decode_workspace_reused_across_shapes(nc):
+    """One workspace, calls with different (B, Hkv): a small call leaves split partials where a larger call's
+    arrival counters go.  The caller-side contract (zero the workspace when B*Hkv changes) and the binding's cached
+    workspace both keep the results exact."""
+    shapes = [(3, 4, 2, 300, [5, 200, 299]), (9, 12, 4, 300, [1, 50, 130, 260, 299, 7, 140, 256, 280]),
+              (2, 8, 1, 300, [299, 180])]
+    for B, Hq, Hkv, Tcap, lens in shapes * 2:
+        out, exp, *_ = decode_case(nc, B, Hq, Hkv, Tcap, lens, -1, False, seed=B)
+        assert_close(out, exp, f"decode B={B} Hkv={Hkv} after other shapes")
+    ws = torch.zeros(nc.nc_attn_decode_workspace_bytes(9, 12, 4, 128, 300, -1), dtype=torch.uint8, device="cuda")
+    prev = None
+    for B, Hq, Hkv, Tcap, lens in shapes * 2:
+        if prev is not None and prev != B * Hkv:
+            ws.zero_()
+        prev = B * Hkv
+        d = decode_inputs(B, Hq, Hkv, 128, Tcap, 1, 2, seed=B)
+        lt = torch.tensor(lens, dtype=torch.int32)
+        exp, _ = ref.attn_decode(f64(d["q"]), f64(d["kcache"]), f64(d["vcache"]), lt.numpy(), -1)
+        out = nc.nc_attn_decode(*cuda(d["q"], d["kcache"], d["vcache"]), lt.cuda(), window=-1, workspace=ws)
+        assert_close(out, exp, f"decode caller workspace B={B} Hkv={Hkv}")
+        # the entry point without a workspace argument (library-held buffer), through the raw C ABI
+        import ctypes
+        qd, kd, vd, ld = cuda(d["q"], d["kcache"], d["vcache"], lt)
+        out2 = torch.empty_like(qd)
+        p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+        st = nc.lib.nc_attn_decode(p(qd), p(kd), p(vd), p(ld), p(out2), None, None, B, Hq, Hkv, 128, Tcap, -1,
+                                   1e5, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == nc.NC_OK
+        assert_close(out2, exp, f"decode library workspace B={B} Hkv={Hkv}")
+
+
 def test_decode_bad_cache_length_sets_status_and_zero_row(nc):
     d = decode_inputs(3, 4, 2, 128, 64, 1, 60, seed=4, with_new=True)
     lens = torch.tensor([10, 64, -1], dtype=torch.int32)   # 64 = Tcap: no room for the new key

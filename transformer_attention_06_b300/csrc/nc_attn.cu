@@ -115,6 +115,7 @@ nc_status launch_prologue(const void* q, const void* k, void* qn, void* kn, int 
 struct HeldBuffer {
   void* ptr = nullptr;
   size_t bytes = 0;
+  long long tag = -1;  // decode: B * Hkv of the last call (its counter region); -1 = freshly zeroed
 };
 
 std::mutex g_ws_mu;
@@ -122,7 +123,10 @@ HeldBuffer g_fwd_ws[16];
 HeldBuffer g_dec_ws[16];
 
 // Returns a buffer of at least `bytes` for the current device, grown in stream order; `zero` clears a new buffer.
-void* held_workspace(HeldBuffer* table, size_t bytes, bool zero, cudaStream_t stream) {
+// `tag` / `clear_bytes`: when a reused buffer was last used with another tag, its first `clear_bytes` are cleared
+// (decode: a call with another B * Hkv may have left split partials where this call's arrival counters live).
+void* held_workspace(HeldBuffer* table, size_t bytes, bool zero, long long tag, size_t clear_bytes,
+                     cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return nullptr;
   std::lock_guard<std::mutex> lock(g_ws_mu);
@@ -136,6 +140,10 @@ void* held_workspace(HeldBuffer* table, size_t bytes, bool zero, cudaStream_t st
     if (zero && cudaMemsetAsync(p, 0, bytes, stream) != cudaSuccess) return nullptr;
     hb.ptr = p;
     hb.bytes = bytes;
+    hb.tag = tag;
+  } else if (hb.tag != tag) {
+    if (clear_bytes > 0 && cudaMemsetAsync(hb.ptr, 0, clear_bytes, stream) != cudaSuccess) return nullptr;
+    hb.tag = tag;
   }
   return hb.ptr;
 }
@@ -271,7 +279,7 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* out, in
   const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
   if (st != NC_OK) return st;
   const size_t need = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
-  void* ws = held_workspace(g_fwd_ws, need, false, stream);
+  void* ws = held_workspace(g_fwd_ws, need, false, -1, 0, stream);
   if (ws == nullptr) return NC_ERR_CUDA;
   return nc_attn_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, ws, need, stream);
 }
@@ -338,8 +346,9 @@ nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* c
   const nc_status st =
       check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
   if (st != NC_OK) return st;
-  const size_t need = decode_layout(B, Hq, Hkv, Tcap, window).total;
-  void* ws = held_workspace(g_dec_ws, need, true, stream);
+  const DecodeLayout L = decode_layout(B, Hq, Hkv, Tcap, window);
+  const size_t need = L.total;
+  void* ws = held_workspace(g_dec_ws, need, true, static_cast<long long>(B) * Hkv, L.off_ml, stream);
   if (ws == nullptr) return NC_ERR_CUDA;
   return nc_attn_decode_ws(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window,
                            rope_base, ws, need, stream);

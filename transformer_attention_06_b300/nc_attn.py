@@ -102,7 +102,10 @@ def _need(t, name, ndim, dtype=torch.bfloat16):
 
 
 # Workspaces cached per (device, kind); the decode one starts zero-filled and every call leaves its counters zero.
+# A decode call with another B * Hkv than the previous one may find the previous call's partials where its counters
+# go, so the cached decode workspace is cleared when B * Hkv changes.
 _ws_cache = {}
+_ws_decode_tag = {}
 
 
 def _workspace(kind, nbytes, device, zero):
@@ -199,6 +202,10 @@ def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=No
     nbytes = nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, int(window))
     if workspace is None:
         workspace = _workspace("decode", nbytes, q.device, zero=True)
+        key = workspace.data_ptr()
+        if _ws_decode_tag.get(key, B * Hkv) != B * Hkv:
+            workspace.zero_()
+        _ws_decode_tag[key] = B * Hkv
     st = lib.nc_attn_decode_ws(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
                                _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
