@@ -46,7 +46,8 @@ typedef enum {
   NC_ERR_CUDA = 3,             /* a CUDA runtime / driver call or a kernel launch failed */
   NC_ERR_DEVICE_TIMEOUT = 4,   /* a bounded wait inside a kernel ran out (see nc_attn_get_device_status) */
   NC_ERR_DEVICE_BAD_INPUT = 5, /* a kernel found an invalid cache length (see nc_attn_get_device_status) */
-  NC_ERR_WORKSPACE = 6         /* the caller's workspace is null or smaller than the *_workspace_bytes value */
+  NC_ERR_WORKSPACE = 6,        /* the caller's workspace is null or smaller than the *_workspace_bytes value */
+  NC_ERR_SCRATCH_LIMIT = 7     /* nc_attn_decode_noalloc: the request needs more than its fixed scratch array */
 } nc_status;
 
 /* ---- prefill / training forward ------------------------------------------------------------------------------
@@ -114,6 +115,33 @@ nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int
 nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
                          const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap, int window,
                          float rope_base, cudaStream_t stream);
+
+/* ---- decode that allocates nothing ----------------------------------------------------------------------------
+ * Not a step of the attention block itself (the pages have no counterpart): an extra way to call the decode step
+ * for callers that may not allocate device memory at all.  Examples: code that runs inside another framework's
+ * plugin or enqueue hook, where the host framework owns the whole memory budget and forbids allocation on the hot
+ * path; serving loops that reserve every byte at start-up, because cudaMalloc and cudaFree can synchronize the
+ * device and stall the other streams.  Such a caller can pass neither a workspace nor let nc_attn_decode grow one.
+ *
+ * Same arguments and results as nc_attn_decode.  The split partials and arrival counters live in one array of
+ * NC_ATTN_DECODE_NOALLOC_MAX_BYTES bytes that the library declares in device memory at file scope; every GPU that
+ * loads the library holds that array until the process exits.  A request fits when
+ * nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window) <= NC_ATTN_DECODE_NOALLOC_MAX_BYTES (the 64-sequence,
+ * Hq 12, Hkv 4, window 2048 decode needs about 6.5 MiB); a larger one returns NC_ERR_SCRATCH_LIMIT and launches
+ * nothing.  The call never runs cudaMalloc, cudaFree or any other allocating routine.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that device
+ *     current) and keeps it; make that first call before any stream capture begins.
+ *   - Each call clears the counter region of the array on `stream` (cudaMemsetAsync) before its kernel, so the
+ *     previous call's leftovers do not matter.
+ *   - All calls on a device share the one array: two calls that overlap on the GPU (different streams without
+ *     ordering between them) race on it and give wrong results.  Order them on one stream, or use nc_attn_decode_ws
+ *     with a workspace per stream.
+ */
+#define NC_ATTN_DECODE_NOALLOC_MAX_BYTES (8u * 1024u * 1024u)
+
+nc_status nc_attn_decode_noalloc(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                                 const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
+                                 int window, float rope_base, cudaStream_t stream);
 
 /* ---- status ------------------------------------------------------------------------------------------------------ */
 /* Static description of a status code (never NULL). */

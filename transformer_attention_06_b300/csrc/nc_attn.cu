@@ -363,6 +363,9 @@ const char* nc_attn_status_string(nc_status s) {
     case NC_ERR_DEVICE_TIMEOUT: return "NC_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
     case NC_ERR_DEVICE_BAD_INPUT: return "NC_ERR_DEVICE_BAD_INPUT: a kernel found a cache length outside the cache";
     case NC_ERR_WORKSPACE: return "NC_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case NC_ERR_SCRATCH_LIMIT:
+      return "NC_ERR_SCRATCH_LIMIT: the request needs more than the fixed no-allocation scratch array "
+             "(NC_ATTN_DECODE_NOALLOC_MAX_BYTES)";
   }
   return "unknown nc_status";
 }
@@ -401,4 +404,51 @@ extern "C" nc_status nc_attn_selftest_wait_timeout(int limit_us, cudaStream_t st
   if (limit_us < 1 || limit_us > 2000000) return NC_ERR_INVALID_ARG;
   nc::selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(limit_us) * 1000ull);
   return launch_status();
+}
+
+// =================================================================================================================
+// Decode without any allocation: the split partials and arrival counters go to a fixed array in device memory,
+// declared here at file scope, instead of a workspace.  For callers that may not allocate (a host framework's plugin
+// hook that owns the memory budget; serving loops that forbid cudaMalloc / cudaFree after start-up because those
+// calls can synchronize the device).  Every GPU that loads the library holds the array until the process exits.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[NC_ATTN_DECODE_NOALLOC_MAX_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[16] = {};
+
+// Device address of the scratch array on the current device.  In host code `g_decode_noalloc_scratch` names a
+// host-side stand-in, not device memory, so the address is looked up once per device (with that device current)
+// and kept.  Returns nullptr when the lookup fails.
+void* noalloc_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+    g_noalloc_addr[dev] = ptr;
+  }
+  return g_noalloc_addr[dev];
+}
+
+}  // namespace
+
+extern "C" nc_status nc_attn_decode_noalloc(const void* q, void* kcache, void* vcache, const int* cache_lens,
+                                            void* out, const void* k_new, const void* v_new, int B, int Hq,
+                                            int Hkv, int D, int Tcap, int window, float rope_base,
+                                            cudaStream_t stream) {
+  const nc_status st =
+      check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
+  if (st != NC_OK) return st;
+  const DecodeLayout L = decode_layout(B, Hq, Hkv, Tcap, window);
+  if (L.total > static_cast<size_t>(NC_ATTN_DECODE_NOALLOC_MAX_BYTES)) return NC_ERR_SCRATCH_LIMIT;
+  void* scratch = noalloc_scratch_address();
+  if (scratch == nullptr) return NC_ERR_CUDA;
+  // The arrival counters at the start of the array must read zero.  A previous call with another B * Hkv may have
+  // left split partials there, so clear the whole counter region in stream order before the kernel.
+  if (cudaMemsetAsync(scratch, 0, L.off_ml, stream) != cudaSuccess) return NC_ERR_CUDA;
+  return nc_attn_decode_ws(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window,
+                           rope_base, scratch, NC_ATTN_DECODE_NOALLOC_MAX_BYTES, stream);
 }

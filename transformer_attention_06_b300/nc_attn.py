@@ -23,6 +23,7 @@ NC_ERR_CUDA = 3
 NC_ERR_DEVICE_TIMEOUT = 4
 NC_ERR_DEVICE_BAD_INPUT = 5
 NC_ERR_WORKSPACE = 6
+NC_ERR_SCRATCH_LIMIT = 7
 
 
 class NcAttnError(RuntimeError):
@@ -45,6 +46,7 @@ def _load():
         "nc_attn_decode_workspace_bytes": (sz, [i, i, i, i, i, i]),
         "nc_attn_decode_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp]),
         "nc_attn_decode": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
+        "nc_attn_decode_noalloc": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
         "nc_attn_status_string": (ctypes.c_char_p, [i]),
         "nc_attn_get_device_status": (i, [vp, i]),
         "nc_attn_selftest_wait_timeout": (i, [i, vp]),
@@ -210,6 +212,45 @@ def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=No
                                _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nc_attn_decode")
+    return out
+
+
+# Largest decode workspace that nc_attn_decode_noalloc can serve from its fixed device array (bytes).
+NC_ATTN_DECODE_NOALLOC_MAX_BYTES = 8 * 1024 * 1024
+
+
+def nc_attn_decode_noalloc(q, kcache, vcache, cache_lens, out, k_new=None, v_new=None, window=-1,
+                           rope_base=ROPE_BASE, stream=None):
+    """Single-token decode that allocates nothing, for callers that may not allocate device memory.
+
+    Same arguments and results as ``nc_attn_decode``, except that ``out`` must be given: the split partials live in
+    a fixed device array of NC_ATTN_DECODE_NOALLOC_MAX_BYTES bytes inside the library, shared by every call on the
+    device, so calls that overlap on the GPU race.  Requests needing a larger workspace raise NcAttnError with
+    NC_ERR_SCRATCH_LIMIT.  Make the first call on a device before any stream capture (it looks up the array's
+    address).
+    """
+    _need(q, "q", 3)
+    _need(kcache, "kcache", 4)
+    _need(vcache, "vcache", 4)
+    _need(cache_lens, "cache_lens", 1, dtype=torch.int32)
+    _need(out, "out", 3)
+    B, Hq, D = q.shape
+    _, Tcap, Hkv, _ = kcache.shape
+    if tuple(kcache.shape) != (B, Tcap, Hkv, D) or tuple(vcache.shape) != (B, Tcap, Hkv, D):
+        raise ValueError("cache shapes do not match q")
+    if cache_lens.shape[0] != B or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("cache_lens must have B entries and out the shape of q")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        _need(k_new, "k_new", 3)
+        _need(v_new, "v_new", 3)
+        if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+            raise ValueError("k_new / v_new must be [B, Hkv, D]")
+    st = lib.nc_attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
+                                    _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base),
+                                    _stream(stream))
+    _check(st, "nc_attn_decode_noalloc")
     return out
 
 
