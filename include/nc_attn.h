@@ -95,7 +95,7 @@ nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, 
  *   out:[B,Hq,D]
  * Visible keys are j in [max(0, p_b - window), L_b) with L_b = p_b (+1 with a new key); window -1 = all.
  * An empty visible set (p_b = 0 and no new key) gives a zero output row and no error.  A p_b outside the cache
- * gives a zero output row and NC_ERR_DEVICE_BAD_INPUT in the device status word.  Requires Hq/Hkv <= 8.
+ * gives a zero output row and NC_ERR_DEVICE_BAD_INPUT in the device status word.  Requires Hq/Hkv <= 16.
  *
  * nc_attn_decode_ws takes a caller-owned device workspace of at least nc_attn_decode_workspace_bytes(...) bytes,
  * 16-byte aligned.  It holds B*Hkv arrival counters at its start, then the split partial results.  The counters
@@ -127,8 +127,8 @@ nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* c
  * NC_ATTN_DECODE_NOALLOC_MAX_BYTES bytes that the library declares in device memory at file scope; every GPU that
  * loads the library holds that array until the process exits.  A request fits when
  * nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window) <= NC_ATTN_DECODE_NOALLOC_MAX_BYTES (the 64-sequence,
- * Hq 12, Hkv 4, window 2048 decode needs about 6.5 MiB); a larger one returns NC_ERR_SCRATCH_LIMIT and launches
- * nothing.  The call never runs cudaMalloc, cudaFree or any other allocating routine.
+ * Hq 12, Hkv 4 decode needs about 0.8 MiB; the size grows with B * Hkv and the group size); a larger one returns
+ * NC_ERR_SCRATCH_LIMIT and launches nothing.  The call never runs cudaMalloc, cudaFree or any other allocating routine.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with that device
  *     current) and keeps it; make that first call before any stream capture begins.
  *   - Each call clears the counter region of the array on `stream` (cudaMemsetAsync) before its kernel, so the

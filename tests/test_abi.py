@@ -94,7 +94,7 @@ def test_decode_rejects_bad_arguments(nc):
     assert dec(nc, W=-5) == E
     assert dec(nc, base=float("inf")) == E
     assert dec(nc, D=256) == U
-    assert dec(nc, Hq=36, Hkv=4) == U           # group of 9 > 8
+    assert dec(nc, Hq=68, Hkv=4) == U           # group of 17 > 16
     assert dec(nc) == WS
     need = nc.nc_attn_decode_workspace_bytes(4, 12, 4, 128, 64, -1)
     assert dec(nc, ws=P, wsb=need - 1) == WS
@@ -104,11 +104,13 @@ def test_workspace_sizes(nc):
     # qn + kn in bf16 plus a small pad
     assert nc.nc_attn_fwd_workspace_bytes(4, 2048, 6, 6) >= 2 * 4 * 2048 * 12 * 128
     assert nc.nc_attn_fwd_workspace_bytes(0, 2048, 6, 6) == 0
-    # decode: counters + (m, l) + 128 floats per (b, kv head, chunk, group head); 17 chunks of 128 for window 2048
+    # decode: B*Hkv counters + (m, l) and 128 floats for 2 partials per CTA (at most 256 CTAs) and group head;
+    # independent of the cache length and window
     n = nc.nc_attn_decode_workspace_bytes(64, 12, 4, 128, 4097, 2048)
-    assert n >= 64 * 4 * 17 * 3 * 130 * 4
-    assert nc.nc_attn_decode_workspace_bytes(64, 12, 4, 128, 4097, 2048) > \
-        nc.nc_attn_decode_workspace_bytes(64, 12, 4, 128, 4097, 100)
+    assert n >= 64 * 4 * 4 + 256 * 2 * 3 * 130 * 4
+    assert n == nc.nc_attn_decode_workspace_bytes(64, 12, 4, 128, 100, 100)
+    assert nc.nc_attn_decode_workspace_bytes(128, 12, 4, 128, 4097, 2048) > n
+    assert nc.nc_attn_decode_workspace_bytes(64, 12, 2, 128, 4097, 2048) > n   # larger group
     assert nc.nc_attn_decode_workspace_bytes(64, 12, 4, 64, 4097, 2048) == 0
 
 

@@ -171,11 +171,46 @@ def test_decode_small(nc, W, with_new):
         assert torch.count_nonzero(out[0]) == 0       # empty visible set
 
 
-@pytest.mark.parametrize("G", [1, 2, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 8, 12, 16])
 def test_decode_group_sizes(nc, G):
     lens = [3, 500, 1000]
     out, exp, *_ = decode_case(nc, 3, 2 * G, 2, 1024, lens, 300, True, seed=G)
     assert_close(out, exp, f"decode G={G}")
+
+
+@pytest.mark.parametrize("W", [-1, 700])
+@pytest.mark.parametrize("with_new", [False, True])
+def test_decode_many_sequences_mixed_lengths(nc, W, with_new):
+    """Hundreds of (sequence, kv head) segments of every length, so that CTA ranges start and end inside segments,
+    some segments span several CTAs and some CTAs hold many short segments."""
+    rng = np.random.default_rng(11)
+    B, Tcap = 300, 2100
+    lens = rng.integers(0, Tcap, size=B)
+    lens[:8] = [0, 1, 127, 128, 129, 2099, 256, 0]
+    out, exp, *_ = decode_case(nc, B, 8, 2, Tcap, lens.tolist(), W, with_new, seed=21)
+    assert_close(out, exp, f"decode mixed lengths W={W} new={with_new}")
+
+
+@pytest.mark.parametrize("L", [129, 5000, 19999])
+def test_decode_one_long_sequence_split_over_ctas(nc, L):
+    """One segment cut into many CTA ranges (up to one tile each): many partials merged by the last CTA."""
+    out, exp, *_ = decode_case(nc, 1, 4, 1, 20000, [L], -1, True, seed=L)
+    assert_close(out, exp, f"decode one sequence L={L}")
+
+
+def test_decode_ignores_garbage_past_the_cache_length(nc):
+    """Cache rows at and after cache_lens[b] may hold anything (here NaN): they must not reach the output."""
+    B, Hq, Hkv, Tcap = 4, 6, 2, 400
+    lens = [1, 100, 130, 300]
+    d = decode_inputs(B, Hq, Hkv, 128, Tcap, 1, 2, seed=8)
+    kc, vc = d["kcache"].clone(), d["vcache"].clone()
+    for b, p in enumerate(lens):
+        kc[b, p:] = float("nan")
+        vc[b, p:] = float("nan")
+    lt = torch.tensor(lens, dtype=torch.int32)
+    exp, _ = ref.attn_decode(f64(d["q"]), f64(d["kcache"]), f64(d["vcache"]), lt.numpy(), -1)
+    out = nc.nc_attn_decode(*cuda(d["q"], kc, vc), lt.cuda(), window=-1)
+    assert_close(out, exp, "decode with NaN past the cache length")
 
 
 def test_decode_full_config(nc):
@@ -227,7 +262,8 @@ def test_decode_workspace_reused_across_shapes(nc):
     for B, Hq, Hkv, Tcap, lens in shapes * 2:
         out, exp, *_ = decode_case(nc, B, Hq, Hkv, Tcap, lens, -1, False, seed=B)
         assert_close(out, exp, f"decode B={B} Hkv={Hkv} after other shapes")
-    ws = torch.zeros(nc.nc_attn_decode_workspace_bytes(9, 12, 4, 128, 300, -1), dtype=torch.uint8, device="cuda")
+    nbytes = max(nc.nc_attn_decode_workspace_bytes(B, Hq, Hkv, 128, Tcap, -1) for B, Hq, Hkv, Tcap, _ in shapes)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     prev = None
     for B, Hq, Hkv, Tcap, lens in shapes * 2:
         if prev is not None and prev != B * Hkv:

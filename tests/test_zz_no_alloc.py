@@ -28,7 +28,7 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     # Checked on the host before any CUDA call: a non-null, aligned dummy address is never dereferenced.
     nc = _nc()
     P = 0x10000
-    B, Hq, Hkv, Tcap = 512, 32, 8, 32768
+    B, Hq, Hkv, Tcap = 65535, 64, 64, 4096    # 4 Mi sequence x kv-head arrival counters alone exceed the array
     need = nc.nc_attn_decode_workspace_bytes(B, Hq, Hkv, 128, Tcap, -1)
     assert need > nc.NC_ATTN_DECODE_NOALLOC_MAX_BYTES
     st = nc.lib.nc_attn_decode_noalloc(P, P, P, P, P, None, None, B, Hq, Hkv, 128, Tcap, -1, 1e5, None)

@@ -87,7 +87,7 @@ nc_status check_fwd_shapes(int B, int T, int Hq, int Hkv, int D) {
 
 template <typename F>
 void set_smem_attr_once(F* kernel, int bytes, int slot) {
-  static bool done[16][8] = {};
+  static bool done[16][32] = {};
   static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -149,24 +149,41 @@ void* held_workspace(HeldBuffer* table, size_t bytes, bool zero, long long tag, 
 }
 
 // ---- decode workspace layout ------------------------------------------------------------------------------------
+// [B * Hkv arrival counters][(m, l) of 2 partials per CTA and head][128-float partial outputs of the same].
 struct DecodeLayout {
-  int n_chunks;
   size_t off_cnt, off_ml, off_o, total;
 };
 
-DecodeLayout decode_layout(int B, int Hq, int Hkv, int Tcap, int window) {
+DecodeLayout decode_layout(int B, int Hq, int Hkv) {
   DecodeLayout L;
-  const int G = Hq / Hkv;
-  const long long span = (window < 0) ? Tcap : std::min<long long>(static_cast<long long>(window) + 1, Tcap);
-  L.n_chunks = static_cast<int>((span + nc::dec::kC - 1) / nc::dec::kC);
-  if (L.n_chunks < 1) L.n_chunks = 1;
-  const size_t slots = static_cast<size_t>(B) * Hkv * L.n_chunks * G;
+  const size_t G = static_cast<size_t>(Hq / Hkv);
+  const size_t slots = static_cast<size_t>(nc::dec::kMaxParts) * 2 * G;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   L.off_cnt = 0;
   L.off_ml = up(static_cast<size_t>(B) * Hkv * sizeof(unsigned));
   L.off_o = L.off_ml + up(slots * 2 * sizeof(float));
   L.total = L.off_o + up(slots * 128 * sizeof(float));
   return L;
+}
+
+template <int G>
+void launch_decode_g(int grid, const CUtensorMap& mk, const CUtensorMap& mv, const RopeTable& tab,
+                     const nc::dec::Params& prm, cudaStream_t stream) {
+  set_smem_attr_once(nc::dec::attn_decode_kernel<G>, nc::dec::kSmemBytes, G);
+  nc::dec::attn_decode_kernel<G><<<grid, nc::dec::kThreads, nc::dec::kSmemBytes, stream>>>(mk, mv, tab, prm);
+}
+
+// Resident CTAs of the decode kernel on the current device: one per SM, at most kMaxParts.
+int decode_grid() {
+  static int cached[16] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 0;
+    cached[dev] = n < nc::dec::kMaxParts ? n : nc::dec::kMaxParts;
+  }
+  return cached[dev];
 }
 
 nc_status check_decode_args(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
@@ -184,15 +201,9 @@ nc_status check_decode_args(const void* q, const void* kcache, const void* vcach
   if (!rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
   if (D != 128) return NC_ERR_UNSUPPORTED;
   if (Hq / Hkv > nc::dec::kMaxG) return NC_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hkv * 4 > (1ll << 40)) return NC_ERR_UNSUPPORTED;
   if (B > 65535 || Hkv > 65535 || Tcap >= (1 << 24)) return NC_ERR_UNSUPPORTED;
   return NC_OK;
-}
-
-template <int G>
-void launch_decode_g(dim3 grid, const CUtensorMap& mk, const CUtensorMap& mv, const RopeTable& tab,
-                     const nc::dec::Params& prm, cudaStream_t stream) {
-  set_smem_attr_once(nc::dec::attn_decode_kernel<G>, nc::dec::kSmemBytes, 1 + G);
-  nc::dec::attn_decode_kernel<G><<<grid, nc::dec::kThreads, nc::dec::kSmemBytes, stream>>>(mk, mv, tab, prm);
 }
 
 }  // namespace
@@ -286,7 +297,8 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* out, in
 
 size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, int window) {
   if (B < 1 || Hq < 1 || Hkv < 1 || D != 128 || Tcap < 1 || Hq % Hkv != 0 || window < -1) return 0;
-  return decode_layout(B, Hq, Hkv, Tcap, window).total;
+  if (Hq / Hkv > nc::dec::kMaxG) return 0;
+  return decode_layout(B, Hq, Hkv).total;
 }
 
 nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
@@ -296,12 +308,14 @@ nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int
   const nc_status st =
       check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
   if (st != NC_OK) return st;
-  const DecodeLayout L = decode_layout(B, Hq, Hkv, Tcap, window);
+  const DecodeLayout L = decode_layout(B, Hq, Hkv);
   if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return NC_ERR_WORKSPACE;
+  const int grid = decode_grid();
+  if (grid < 1) return NC_ERR_CUDA;
 
   CUtensorMap mk, mv;
-  if (!make_map_4d(&mk, kcache, 128, Hkv, Tcap, B, 64, 1, nc::dec::kC, 1) ||
-      !make_map_4d(&mv, vcache, 128, Hkv, Tcap, B, 64, 1, nc::dec::kC, 1))
+  if (!make_map_4d(&mk, kcache, 128, Hkv, Tcap, B, 64, 1, nc::dec::kRows, 1) ||
+      !make_map_4d(&mv, vcache, 128, Hkv, Tcap, B, 64, 1, nc::dec::kRows, 1))
     return NC_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -319,14 +333,13 @@ nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
+  prm.G = Hq / Hkv;
   prm.Tcap = Tcap;
   prm.window = window;
-  prm.n_chunks = L.n_chunks;
   prm.scale_log2 = scale_log2_for_d128();
   prm.wait_limit_ns = kWaitLimitNs;
   const RopeTable tab = rope_table(rope_base);
-  const dim3 grid(L.n_chunks, Hkv, B);
-  switch (Hq / Hkv) {
+  switch (prm.G) {
     case 1: launch_decode_g<1>(grid, mk, mv, tab, prm, stream); break;
     case 2: launch_decode_g<2>(grid, mk, mv, tab, prm, stream); break;
     case 3: launch_decode_g<3>(grid, mk, mv, tab, prm, stream); break;
@@ -335,6 +348,14 @@ nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int
     case 6: launch_decode_g<6>(grid, mk, mv, tab, prm, stream); break;
     case 7: launch_decode_g<7>(grid, mk, mv, tab, prm, stream); break;
     case 8: launch_decode_g<8>(grid, mk, mv, tab, prm, stream); break;
+    case 9: launch_decode_g<9>(grid, mk, mv, tab, prm, stream); break;
+    case 10: launch_decode_g<10>(grid, mk, mv, tab, prm, stream); break;
+    case 11: launch_decode_g<11>(grid, mk, mv, tab, prm, stream); break;
+    case 12: launch_decode_g<12>(grid, mk, mv, tab, prm, stream); break;
+    case 13: launch_decode_g<13>(grid, mk, mv, tab, prm, stream); break;
+    case 14: launch_decode_g<14>(grid, mk, mv, tab, prm, stream); break;
+    case 15: launch_decode_g<15>(grid, mk, mv, tab, prm, stream); break;
+    case 16: launch_decode_g<16>(grid, mk, mv, tab, prm, stream); break;
     default: return NC_ERR_UNSUPPORTED;
   }
   return launch_status();
@@ -346,7 +367,7 @@ nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* c
   const nc_status st =
       check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
   if (st != NC_OK) return st;
-  const DecodeLayout L = decode_layout(B, Hq, Hkv, Tcap, window);
+  const DecodeLayout L = decode_layout(B, Hq, Hkv);
   const size_t need = L.total;
   void* ws = held_workspace(g_dec_ws, need, true, static_cast<long long>(B) * Hkv, L.off_ml, stream);
   if (ws == nullptr) return NC_ERR_CUDA;
@@ -442,7 +463,7 @@ extern "C" nc_status nc_attn_decode_noalloc(const void* q, void* kcache, void* v
   const nc_status st =
       check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
   if (st != NC_OK) return st;
-  const DecodeLayout L = decode_layout(B, Hq, Hkv, Tcap, window);
+  const DecodeLayout L = decode_layout(B, Hq, Hkv);
   if (L.total > static_cast<size_t>(NC_ATTN_DECODE_NOALLOC_MAX_BYTES)) return NC_ERR_SCRATCH_LIMIT;
   void* scratch = noalloc_scratch_address();
   if (scratch == nullptr) return NC_ERR_CUDA;
