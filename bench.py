@@ -109,72 +109,73 @@ def cpu_model():
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons of the GPU during the timed region (NVML, else nvidia-smi)."""
+    """Samples SM clock, power and clock-event reasons of the GPU with `nvidia-smi -lms` while the timed region runs.
 
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
-               0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x10: "sync_boost"}
+    Only samples whose nvidia-smi timestamp falls inside [t_begin, t_end] of the timed region are kept (host clock).
+    """
 
-    def __init__(self, device_index):
-        self.samples = []
-        self.reasons = 0
-        self.max_mhz = None
-        self._stop = threading.Event()
-        self._thread = None
-        self._nvml = None
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    FLAGS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index, interval_ms=20):
+        self.proc = None
+        self.lines = []
+        self.interval_ms = interval_ms
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = None
-            try:
-                props = torch.cuda.get_device_properties(device_index)
-                bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
-                h = pynvml.nvmlDeviceGetHandleByPciBusId(bus.encode())
-            except Exception:
-                h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self._nvml = pynvml
-            self._h = h
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            props = torch.cuda.get_device_properties(device_index)
+            self.target = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
         except Exception:
-            self._nvml = None
-
-    def _run(self):
-        pn = self._nvml
-        while not self._stop.is_set():
-            try:
-                self.samples.append(pn.nvmlDeviceGetClockInfo(self._h, pn.NVML_CLOCK_SM))
-                self.reasons |= int(pn.nvmlDeviceGetCurrentClocksEventReasons(self._h))
-            except Exception:
-                try:
-                    self.reasons |= int(pn.nvmlDeviceGetCurrentClocksThrottleReasons(self._h))
-                except Exception:
-                    pass
-            time.sleep(0.002)
+            self.target = str(device_index)
 
     def start(self):
-        if self._nvml is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
-            self._thread.start()
-
-    def stop(self):
-        if self._thread is not None:
-            self._stop.set()
-            self._thread.join()
-        if not self.samples:
-            return self._smi_once()
-        names = sorted(n for bit, n in self.REASONS.items() if self.reasons & bit)
-        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(self.samples), "source": "nvml"}
-
-    @staticmethod
-    def _smi_once():
         try:
-            out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
-                                  "--format=csv,noheader,nounits", "-i", "0"], capture_output=True, text=True,
-                                 timeout=20).stdout.strip().splitlines()[0].split(",")
-            return {"sm_mhz": float(out[0]), "sm_max_mhz": float(out[1]), "reasons": [out[2].strip()],
-                    "samples": 1, "source": "nvidia-smi after the timed region"}
-        except Exception as e:  # noqa: BLE001
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": str(e)}
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._thread = threading.Thread(target=self._read, daemon=True)
+            self._thread.start()
+            time.sleep(0.3)  # let the first samples arrive before the timed region starts
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self, t_begin, t_end):
+        import datetime
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": "nvidia-smi unavailable"}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._thread.join(timeout=5)
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) != len(self.FIELDS):
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]), f[3], f[5:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t_begin - 0.03 <= r[0] <= t_end + 0.03]
+        if not inside and rows:  # timed region shorter than the sampling interval: nearest sample
+            inside = [min(rows, key=lambda r: abs(r[0] - 0.5 * (t_begin + t_end)))]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": "no samples"}
+        reasons = sorted({name for r in inside for name, v in zip(self.FLAGS, r[4]) if v.lower() == "active"})
+        power = [float(r[3]) for r in inside if r[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": float(statistics.median(r[1] for r in inside)), "sm_max_mhz": inside[0][2],
+                "reasons": reasons, "samples": len(inside), "power_w_max": max(power) if power else None,
+                "timed_region_s": round(t_end - t_begin, 4), "source": f"nvidia-smi -lms {self.interval_ms}"}
 
 
 def kernel_traffic(kernel, src_files):
@@ -293,28 +294,46 @@ def run_ours(args, ws, rank, local):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
+    # One step (the four layer calls) captured once as a CUDA graph and replayed per timed step: the device work is
+    # the same as an eager step without the host launch gaps between the eight kernels.
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        g_step.replay()
+    torch.cuda.synchronize()
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     step_ev = [(mk(), mk()) for _ in range(args.steps)]
-    k_ev = [[(mk(), mk(), mk()) for _ in layers] for _ in range(args.steps)]
     clocks = ClockSampler(local)
+    clocks.start()
     dist_barrier(ws)
     torch.cuda.synchronize()
-    clocks.start()
+    t_wall0 = time.time()
     for s in range(args.steps):
         flush.fill_(s & 0xFF)
         step_ev[s][0].record(stream)
-        step(k_ev[s])
+        g_step.replay()
         step_ev[s][1].record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    t_wall1 = time.time()
+    clk = clocks.stop(t_wall0, t_wall1)
     dist_barrier(ws)
     total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     total_ms_max = dist_max(total_ms, ws)
     value = ws * args.steps * flops_step / (total_ms_max * 1e-3) / 1e12
+
+    # Kernel times for the roofline: eager steps with CUDA events recorded on the stream around each kernel.
+    n_roof = min(args.steps, 50)
+    k_ev = [[(mk(), mk(), mk()) for _ in layers] for _ in range(n_roof)]
+    for s in range(n_roof):
+        flush.fill_(s & 0xFF)
+        step(k_ev[s])
+    torch.cuda.synchronize()
     k2_ms = [[e[1].elapsed_time(e[2]) for e in row] for row in k_ev]
     k1_ms = [[e[0].elapsed_time(e[1]) for e in row] for row in k_ev]
     k2_total = sum(sum(r) for r in k2_ms)
-    k2_flops = args.steps * flops_step
+    k2_flops = n_roof * flops_step
     achieved = k2_flops / (k2_total * 1e-3) / 1e12
     traffic = kernel_traffic("attn_fwd_kernel", ["transformer_attention_06_b300/csrc/attn_fwd.cuh",
                                                  "transformer_attention_06_b300/csrc/common.cuh"])
@@ -360,18 +379,28 @@ def run_ours(args, ws, rank, local):
             dws = torch.zeros(nc.nc_attn_decode_workspace_bytes(dw.B, dw.Hq, dw.Hkv, dw.D, dw.Tcap, dw.window),
                               dtype=torch.uint8, device=dev)
             nbytes = decode_bytes(d["cache_lens"].tolist(), dw.window, dw.B, dw.Hq, dw.Hkv, dw.D, with_new)
-            n_dec = max(40, args.steps)
+            n_dec = 40
             for i in range(max(3, args.warmup)):
                 kc, vc = copies[i % 4]
                 nc.nc_attn_decode(qd, kc, vc, lens, out, kn, vn, window=dw.window, workspace=dws)
             torch.cuda.synchronize()
+            # 40 calls over the 4 rotated cache copies, captured once and replayed: device time per call without
+            # host launch gaps (one call is far shorter than the host side of a launch).
+            g_dec = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_dec):
+                for i in range(n_dec):
+                    kc, vc = copies[i % 4]
+                    nc.nc_attn_decode(qd, kc, vc, lens, out, kn, vn, window=dw.window, workspace=dws)
+            g_dec.replay()
+            torch.cuda.synchronize()
             a, b = mk(), mk()
+            reps = 3
             a.record(stream)
-            for i in range(n_dec):
-                kc, vc = copies[i % 4]
-                nc.nc_attn_decode(qd, kc, vc, lens, out, kn, vn, window=dw.window, workspace=dws)
+            for _ in range(reps):
+                g_dec.replay()
             b.record(stream)
             torch.cuda.synchronize()
+            n_dec *= reps
             us = dist_max(a.elapsed_time(b) * 1e3 / n_dec, ws)
             gbs = nbytes / (us * 1e-6) / 1e9
             dec["with_new" if with_new else "cache_only"] = {
@@ -380,7 +409,8 @@ def run_ours(args, ws, rank, local):
             del copies
             torch.cuda.empty_cache()
         dec["config"] = (f"{dw.name}: B={dw.B} Hq={dw.Hq} Hkv={dw.Hkv} D={dw.D} Tcap={dw.Tcap} window={dw.window}, "
-                         f"cache lengths U[{dw.len_lo},{dw.len_hi}] seed 0; 4 rotated cache copies (> L2)")
+                         f"cache lengths U[{dw.len_lo},{dw.len_hi}] seed 0; 4 rotated cache copies (> L2); "
+                         f"calls replayed from a CUDA graph")
         dec["peak_gbs"] = peaks["hbm_gbs"]
 
     st = nc.nc_attn_get_device_status(clear=True)
@@ -396,6 +426,8 @@ def run_ours(args, ws, rank, local):
             "config": {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hkv={w.Hkv} D={w.D}, one step = SSSL "
                                    f"layers with windows {list(w.windows)}, distinct seeded q,k,v per layer",
                        "l2": "512 MiB write before every timed step, outside the timed events",
+                       "timing": "each step replayed from a CUDA graph of its eight kernels; kernel times for the "
+                                 "roofline from CUDA events around each kernel in eager steps",
                        "flops_per_step": flops_step, "parallelism": f"replicas x{ws}"},
             "frac_of_bf16_peak": value / ws / peaks["bf16_tflops"],
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved,
@@ -404,8 +436,9 @@ def run_ours(args, ws, rank, local):
                          "traffic": traffic, "peak_source": f"{peak_src} bf16 dense (burst)",
                          "achieved_def": "sum of in-band FLOPs of the attention-kernel launches / sum of their "
                                          "CUDA-event durations",
-                         "us_per_launch": 1e3 * k2_total / (args.steps * len(layers)),
-                         "prologue_us_per_launch": 1e3 * sum(sum(r) for r in k1_ms) / (args.steps * len(layers))},
+                         "us_per_launch": 1e3 * k2_total / (n_roof * len(layers)),
+                         "prologue_us_per_launch": 1e3 * sum(sum(r) for r in k1_ms) / (n_roof * len(layers)),
+                         "launches_timed": n_roof * len(layers)},
             "decode": dec,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -419,7 +452,7 @@ def run_ours(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-decode", action="store_true")
