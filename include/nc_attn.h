@@ -148,8 +148,9 @@ nc_status nc_attn_decode_noalloc(const void* q, void* kcache, void* vcache, cons
 const char* nc_attn_status_string(nc_status s);
 
 /* Synchronizes `stream`, then returns the sticky device status of the current device (NC_OK when clean,
- * NC_ERR_DEVICE_TIMEOUT or NC_ERR_DEVICE_BAD_INPUT otherwise; timeout wins) and, when `clear` is non-zero,
- * resets it.  Returns NC_ERR_CUDA when the synchronization or the read fails. */
+ * NC_ERR_DEVICE_TIMEOUT or NC_ERR_DEVICE_BAD_INPUT otherwise; timeout wins; NC_ERR_UNSUPPORTED if a kernel found
+ * its dynamic shared memory less aligned than it can use, in which case it wrote nothing) and, when `clear` is
+ * non-zero, resets it.  Returns NC_ERR_CUDA when the synchronization or the read fails. */
 nc_status nc_attn_get_device_status(cudaStream_t stream, int clear);
 
 /* Self-test of the bounded waits: launches one tiny kernel whose threads wait on a barrier that nothing ever

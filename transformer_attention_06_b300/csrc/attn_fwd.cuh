@@ -4,19 +4,34 @@
 // g = h / G, out = softmax_j(qn . kn_j / sqrt(D)) . v_j over the visible keys j (j <= t, and t - j <= window when
 // window >= 0).  qn / kn are the roped + normed vectors written by K1.
 //
-// Tiling.  One CTA owns one tile of 128 MMA rows: P = 128 / G consecutive query positions times the G query heads
-// of kv head g (row r = position (r / G), head (r % G)), so every K/V tile brought in by TMA is shared by the whole
-// GQA group.  Keys are processed in tiles of 128; only tiles that intersect the causal / window band of the query
-// tile are visited, and only tiles that straddle the band edge pay for the element mask.
+// Tiling.  A Q tile is 128 MMA rows: P = 128 / G consecutive query positions times the G query heads of kv head g
+// (row r = position r / G, head r % G), so every K/V tile brought in by TMA serves the whole GQA group.  A work item
+// is two consecutive Q tiles (A and B) of one (b, g): every K/V tile is loaded once for both.  Keys are processed
+// in tiles of 128; a Q tile only visits the key tiles that intersect its causal / window band, and only tiles that
+// straddle the band edge pay for the element mask.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread r owns TMEM lane r = query row r; online softmax in the log2 domain, writes P
-//              (bf16) over its S row in TMEM, rescales its O row when the row maximum grows, and runs the epilogue;
-//   warp 4     TMA producer: Q tile once, then K and V tiles through a 2-stage ring;
-//   warp 5     TMEM allocator and MMA issuer (one thread): S = Q K^T into one of two S buffers, O += P V with P read
-//              from TMEM (A operand) and V from shared memory (MN-major B operand).
-// TMEM (512 columns): S0 = [0,128), S1 = [128,256), O = [256,384); P_i overlays the first 64 columns of S_i.
-// Shared memory: Q 32 KB + 2 x (K 32 KB + V 32 KB), all in the 128-byte-swizzled K-major layout written by TMA.
+// Persistent grid: one CTA per SM takes work items from a global counter (zeroed by the prologue kernel), the
+// latest (heaviest under a causal mask) Q tiles first, so the tail of the launch is made of the lightest items.
+//
+// Warp roles (384 threads, three warpgroups; launched at 168 registers per thread, the softmax warpgroups take 208
+// and the third warpgroup keeps 88: 2 x 128 x 208 + 128 x 88 = 384 x 168):
+//   warps 0-7   softmax and epilogue.  Both Q tiles are handled by all eight warps, one tile at a time (A, then B,
+//               in every key-tile round), so each tile's softmax runs alone on the exponential and issue units
+//               while the tensor core works on the other tile.  Thread (warp w, lane) owns row r = 32 (w % 4) + lane
+//               (= TMEM lane r) and the column half h = w / 4: exponentials of its 64 scores against the fixed
+//               offset kScoreBound (below), P (bf16) written over its part of the S row in TMEM, and its half of the
+//               epilogue.  The two halves of a row combine their row sums only in the epilogue, which writes
+//               O / l into a shared-memory staging tile that one thread sends out with a TMA store;
+//   warp 8      TMA producer and scheduler: fetches work items and serves three queues in whichever order their
+//               buffers free up -- Q_A, Q_B once per item, K and V tiles through 2-stage rings;
+//   warps 9, 10 MMA issuers, one per Q tile X (warp 9 also allocates TMEM; warp 11 idle): per key tile j,
+//               O_X += P_X(j) V_j then S_X = Q_X K_{j+1}^T.  The two tiles' chains are independent (disjoint TMEM,
+//               and a commit only tracks its own thread's MMAs), so the tensor core serves whichever tile is ready
+//               while the other tile's softmax runs.  K, V stages and the Q tiles are released by one commit from
+//               each issuer (barriers of count 2).
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512); P_X overlays the first 64
+// columns of S_X.  Shared memory: Q_A, Q_B 32 KB each, 2-stage K and V rings of 32 KB tiles, all in the
+// 128-byte-swizzled K-major layout written by TMA, and one 32 KB output staging tile in the same layout.
 #pragma once
 
 #include <climits>
@@ -28,78 +43,168 @@ namespace fwd {
 
 constexpr int kD = 128;
 constexpr int kBlockN = 128;                  // keys per KV tile
-constexpr int kStages = 2;
+constexpr int kKStages = 2;                   // K ring: a stage is free once both S products of its tile are done
+constexpr int kVStages = 2;                   // V ring: a stage is free once both P.V products of its tile are done
 constexpr int kHalfBytes = 128 * 128;         // one 64-column half of a 128-row bf16 tile
 constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kSoftThreads = 128;             // one warpgroup per Q tile
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;                   // MMA issuer of Q tile A; also allocates TMEM
+constexpr int kMmaWarpB = 10;                 // MMA issuer of Q tile B
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsSoftmax = 208, kRegsOther = 88;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColS = 0;                 // S_X at kColS + 128 X
+constexpr uint32_t kColO = 256;               // O_X at kColO + 128 X
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);  // A = Q, B = K, both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // A = P (TMEM), B = V (MN-major)
+// Fixed softmax offset.  qn and kn are RMS-normalised by the prologue (RMSNorm without weight, eps > 0), so
+// |qn| <= sqrt(128) and |kn| <= sqrt(128) before rounding to bf16 and <= sqrt(128) (1 + 2^-9) after it; every raw
+// score qn . kn therefore lies in [-129, 129] (128 (1 + 2^-9)^2 < 128.6).  Softmax is invariant under a common
+// shift, so exponentials taken relative to this bound instead of the running row maximum give the same result:
+// 2^((s - 130) log2(e) / sqrt(128)) lies in [2^-33, 1], far from fp32 and bf16 underflow, and neither O nor the
+// row sums ever need rescaling.
+constexpr float kScoreBound = 130.f;
 
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kOffMisc = kOffBar + 16 * 8;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;   // + slack to align the base to 1024 bytes
+constexpr int kOffQ = 0;                                 // Q_A, Q_B
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffO = kOffV + kVStages * kTileBytes;    // output staging of one Q tile (TMA store source)
+constexpr int kOffBar = kOffO + kTileBytes;
+// mbarrier slots (each 8 bytes), derived from the ring depths so that no two barriers can overlap.
+constexpr int kBarKFull = 0;
+constexpr int kBarKEmpty = kBarKFull + kKStages;
+constexpr int kBarVFull = kBarKEmpty + kKStages;
+constexpr int kBarVEmpty = kBarVFull + kVStages;
+constexpr int kBarQFull = kBarVEmpty + kVStages;
+constexpr int kBarQEmpty = kBarQFull + 2;
+constexpr int kBarSFull = kBarQEmpty + 1;
+constexpr int kBarPFull = kBarSFull + 2;
+constexpr int kBarODone = kBarPFull + 2;
+constexpr int kBarOFree = kBarODone + 2;
+constexpr int kBarSchedFull = kBarOFree + 2;
+constexpr int kBarSchedEmpty = kBarSchedFull + 2;
+constexpr int kBarMmaFinal = kBarSchedEmpty + 2;   // [2], one per MMA warp
+constexpr int kNumBars = kBarMmaFinal + 2;
+static_assert(kNumBars <= 32, "barrier block");
+constexpr int kOffXch = kOffBar + kNumBars * 8;  // row-sum exchange, [2 halves][128] f32 (1 KB used)
+constexpr int kOffMisc = kOffXch + 2048;
+// The dynamic shared memory base is aligned up to 1024 bytes inside the kernel; 768 bytes of slack cover bases
+// that are at least 256-byte aligned (in practice it is 1024-byte aligned), and the kernel checks this.
+constexpr int kAlignSlack = 768;
+constexpr int kSmemBytes = kOffMisc + 16 + kAlignSlack;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
   __nv_bfloat16* out;
-  int B, T, Hq, Hkv, G, P, n_qtiles, window;
+  unsigned* item_ctr;                 // work-item counter, zero at launch (written by the prologue kernel)
+  int B, T, Hq, Hkv, G, P, n_pairs, n_items, window;
   float scale_log2;                   // log2(e) / sqrt(D)
   unsigned long long wait_limit_ns;
 };
 
+// Key-tile range of one Q tile: tiles [lo, hi] intersect its band; n = 0 when the tile lies past T.
+struct QRange {
+  int t0, t_last, lo, hi, n;
+};
+
+__device__ __forceinline__ QRange q_range(const Params& p, int t0) {
+  QRange q;
+  q.t0 = t0;
+  if (t0 >= p.T) {
+    q.t_last = t0 - 1;
+    q.lo = 0;
+    q.hi = -1;
+    q.n = 0;
+    return q;
+  }
+  q.t_last = min(t0 + p.P, p.T) - 1;
+  const int key_lo = p.window < 0 ? 0 : max(0, t0 - p.window);
+  q.lo = key_lo / kBlockN;
+  q.hi = q.t_last / kBlockN;
+  q.n = q.hi - q.lo + 1;
+  return q;
+}
+
+struct Item {
+  int b, g;
+  QRange qa, qb;
+  int lo, hi;  // union of the two key-tile ranges
+};
+
+__device__ __forceinline__ Item decode_item(const Params& p, int item) {
+  Item it;
+  const int bh = p.B * p.Hkv;
+  const int pair = p.n_pairs - 1 - item / bh;  // latest Q tiles first
+  const int bg = item - (item / bh) * bh;
+  it.b = bg / p.Hkv;
+  it.g = bg - it.b * p.Hkv;
+  it.qa = q_range(p, pair * 2 * p.P);
+  it.qb = q_range(p, pair * 2 * p.P + p.P);
+  it.lo = it.qa.lo;
+  it.hi = it.qb.n > 0 ? max(it.qa.hi, it.qb.hi) : it.qa.hi;
+  return it;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
+  uint8_t* sO = smem + kOffO;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [kStages]
-  uint64_t* v_full = bars + 3;    // [kStages]
-  uint64_t* kv_empty = bars + 5;  // [kStages]
-  uint64_t* s_full = bars + 7;    // [2]  S_i written by the MMA
-  uint64_t* p_full = bars + 9;    // [2]  P_i written (and O rescaled) by the 128 softmax threads
-  uint64_t* o_done = bars + 11;   // one completion per P.V product
-  uint64_t* mma_final = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  uint64_t* k_full = bars + kBarKFull;        // [kKStages]  TMA -> MMA
+  uint64_t* k_empty = bars + kBarKEmpty;      // [kKStages]  MMA -> TMA
+  uint64_t* v_full = bars + kBarVFull;        // [kVStages]  TMA -> MMA
+  uint64_t* v_empty = bars + kBarVEmpty;      // [kVStages]  MMA -> TMA
+  uint64_t* q_full = bars + kBarQFull;        // [2]  Q_A, Q_B of the current item               TMA -> MMA
+  uint64_t* q_empty = bars + kBarQEmpty;      //      every S of the item complete               MMA -> TMA
+  uint64_t* s_full = bars + kBarSFull;        // [2]  S_X written                                MMA -> softmax X
+  uint64_t* p_full = bars + kBarPFull;        // [2]  P_X written, O_X rescaled (256 arrivals)   softmax -> MMA
+  uint64_t* o_done = bars + kBarODone;        // [2]  P_X V product complete                     MMA -> softmax X
+  uint64_t* o_free = bars + kBarOFree;        // [2]  O_X read by the epilogue (256 arrivals)    softmax -> MMA
+  uint64_t* sched_full = bars + kBarSchedFull;    // [2]  work item published                     TMA -> all
+  uint64_t* sched_empty = bars + kBarSchedEmpty;  // [2]  work item read (2 MMA warps + the softmax warps)
+  uint64_t* mma_final = bars + kBarMmaFinal;
+  float* xch = reinterpret_cast<float*>(smem + kOffXch);
+  int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = misc + 1;
+  int* sched = misc + 2;            // [2] work-item ring
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x / p.Hkv;
-  const int g = blockIdx.x - b * p.Hkv;
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // heaviest (latest) query tiles first
-  const int t0 = qt * p.P;
-  const int t_last = min(t0 + p.P, p.T) - 1;
-  const int key_lo = p.window < 0 ? 0 : max(0, t0 - p.window);
-  const int kt0 = key_lo / kBlockN;
-  const int n_kv = t_last / kBlockN - kt0 + 1;
-  const int rows_used = p.G * p.P;
   const unsigned long long lim = p.wait_limit_ns;
+  if (static_cast<int>(smem - smem_raw) > kAlignSlack) {  // uniform: every thread sees the same base
+    if (threadIdx.x == 0) raise_status(NC_DEV_SMEM_BASE);
+    return;
+  }
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 2);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(v_full + s, 1);
-      mbar_init(kv_empty + s, 1);
+      mbar_init(v_empty + s, 2);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(s_full + s, 1);
-      mbar_init(p_full + s, 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(q_full + x, 1);
+      mbar_init(s_full + x, 1);
+      mbar_init(p_full + x, 2 * kSoftThreads);
+      mbar_init(o_done + x, 1);
+      mbar_init(o_free + x, 2 * kSoftThreads);
+      mbar_init(sched_full + x, 1);
+      mbar_init(sched_empty + x, 3);
     }
-    mbar_init(o_done, 1);
-    mbar_init(mma_final, 1);
+    mbar_init(q_empty, 2);
+    mbar_init(mma_final + 0, 1);
+    mbar_init(mma_final + 1, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -107,13 +212,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (threadIdx.x < 128 && static_cast<int>(threadIdx.x) >= rows_used) {
-    // Rows of the Q tile that TMA does not fill (128 is not a multiple of G): zero them so they stay finite.
-    uint4* r0 = reinterpret_cast<uint4*>(sQ + threadIdx.x * 128);
-    uint4* r1 = reinterpret_cast<uint4*>(sQ + kHalfBytes + threadIdx.x * 128);
-    for (int i = 0; i < 8; ++i) {
-      r0[i] = make_uint4(0, 0, 0, 0);
-      r1[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x < 256 && p.G * p.P < 128) {
+    // Rows of the Q tiles that TMA never fills (128 is not a multiple of G): zero them once so they stay finite.
+    const int x = threadIdx.x >> 7, r = threadIdx.x & 127;
+    if (r >= p.G * p.P) {
+      uint4* r0 = reinterpret_cast<uint4*>(sQ + x * kTileBytes + r * 128);
+      uint4* r1 = reinterpret_cast<uint4*>(sQ + x * kTileBytes + kHalfBytes + r * 128);
+      for (int i = 0; i < 8; ++i) {
+        r0[i] = make_uint4(0, 0, 0, 0);
+        r1[i] = make_uint4(0, 0, 0, 0);
+      }
     }
   }
   fence_proxy_async_smem();
@@ -121,196 +229,352 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
-
-  if (warp == kProducerWarp) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- TMA producer
+  const uint32_t q_bytes = 2u * 128u * static_cast<uint32_t>(p.G * p.P);  // one Q tile (box {64, G, P, 1} x 2)
+  if (warp >= 8) {
+    warpgroup_reg_dec<kRegsOther>();
+    if (warp == kProducerWarp && lane == 0) {
+      // ---------------------------------------------------------------- scheduler + TMA producer
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, 2u * 128u * static_cast<uint32_t>(rows_used));
-      tma_load_4d(sQ, &tmQ, q_full, 0, g * p.G, t0, b);
-      tma_load_4d(sQ + kHalfBytes, &tmQ, q_full, 64, g * p.G, t0, b);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (j >= kStages && !mbar_wait(kv_empty + st, ((j >> 1) - 1) & 1, lim, abort_flag)) break;
-        const int s0 = (kt0 + j) * kBlockN;
-        uint8_t* dk = sK + st * kTileBytes;
-        uint8_t* dv = sV + st * kTileBytes;
-        mbar_arrive_expect_tx(k_full + st, kTileBytes);
-        tma_load_4d(dk, &tmK, k_full + st, 0, g, s0, b);
-        tma_load_4d(dk + kHalfBytes, &tmK, k_full + st, 64, g, s0, b);
-        mbar_arrive_expect_tx(v_full + st, kTileBytes);
-        tma_load_4d(dv, &tmV, v_full + st, 0, g, s0, b);
-        tma_load_4d(dv + kHalfBytes, &tmV, v_full + st, 64, g, s0, b);
-        issued = j + 1;
+      tma_prefetch_desc(&tmO);
+      // Items fetched so far live in a 2-slot ring (the same slots the consumers read).  Three cursors walk the
+      // item sequence: Q (item iq), K (item ik, tile jk), V (item iv, tile jv); kt / vt count the K / V tiles
+      // loaded over all items (ring positions).
+      Item items[2];
+      int nfetched = 0;
+      bool done = false;          // the counter ran past the last item
+      int iq = 0, ik = 0, iv = 0, jk = 0, jv = 0, kt = 0, vt = 0;
+      uint64_t t_idle = 0;
+      uint32_t spins = 0;
+      bool ok = true;
+      while (ok) {
+        bool progress = false;
+        // fetch the next item once the K cursor needs it and its slot has been read by every consumer
+        if (!done && ik == nfetched && nfetched - min(iq, iv) < 2 &&
+            (nfetched < 2 || mbar_test(sched_empty + (nfetched & 1), ((nfetched >> 1) - 1) & 1))) {
+          const int slot = nfetched & 1;
+          const int item = static_cast<int>(atomicAdd(p.item_ctr, 1u));
+          sched[slot] = item < p.n_items ? item : -1;
+          mbar_arrive(sched_full + slot);
+          if (item >= p.n_items) {
+            done = true;
+          } else {
+            items[slot] = decode_item(p, item);
+            jk = items[slot].lo;
+            if (nfetched == iv) jv = items[slot].lo;
+            ++nfetched;
+          }
+          progress = true;
+        }
+        // Q tiles of item iq, once every S of item iq - 1 has completed
+        if (iq < nfetched && (iq == 0 || mbar_test(q_empty, (iq - 1) & 1))) {
+          const Item& it = items[iq & 1];
+          mbar_arrive_expect_tx(q_full + 0, q_bytes);
+          tma_load_4d(sQ, &tmQ, q_full + 0, 0, it.g * p.G, it.qa.t0, it.b);
+          tma_load_4d(sQ + kHalfBytes, &tmQ, q_full + 0, 64, it.g * p.G, it.qa.t0, it.b);
+          mbar_arrive_expect_tx(q_full + 1, q_bytes);  // past T the box reads as zeros (still full bytes)
+          tma_load_4d(sQ + kTileBytes, &tmQ, q_full + 1, 0, it.g * p.G, it.qb.t0, it.b);
+          tma_load_4d(sQ + kTileBytes + kHalfBytes, &tmQ, q_full + 1, 64, it.g * p.G, it.qb.t0, it.b);
+          ++iq;
+          progress = true;
+        }
+        // next K tile
+        if (ik < nfetched && (kt < kKStages || mbar_test(k_empty + kt % kKStages, ((kt / kKStages) - 1) & 1))) {
+          const Item& it = items[ik & 1];
+          const int st = kt % kKStages;
+          uint8_t* dk = sK + st * kTileBytes;
+          mbar_arrive_expect_tx(k_full + st, kTileBytes);
+          tma_load_4d(dk, &tmK, k_full + st, 0, it.g, jk * kBlockN, it.b);
+          tma_load_4d(dk + kHalfBytes, &tmK, k_full + st, 64, it.g, jk * kBlockN, it.b);
+          ++kt;
+          if (++jk > it.hi) ++ik;  // the next item's first tile is set when it is fetched
+          progress = true;
+        }
+        // next V tile
+        if (iv < ik || (iv == ik && iv < nfetched && jv < jk)) {
+          if (vt < kVStages || mbar_test(v_empty + vt % kVStages, ((vt / kVStages) - 1) & 1)) {
+            const Item& it = items[iv & 1];
+            const int st = vt % kVStages;
+            uint8_t* dv = sV + st * kTileBytes;
+            mbar_arrive_expect_tx(v_full + st, kTileBytes);
+            tma_load_4d(dv, &tmV, v_full + st, 0, it.g, jv * kBlockN, it.b);
+            tma_load_4d(dv + kHalfBytes, &tmV, v_full + st, 64, it.g, jv * kBlockN, it.b);
+            ++vt;
+            if (++jv > it.hi) {
+              ++iv;
+              if (iv < nfetched) jv = items[iv & 1].lo;
+            }
+            progress = true;
+          }
+        }
+        if (done && iv == nfetched && iq == nfetched) break;
+        if (progress) {
+          spins = 0;
+          continue;
+        }
+        // Bounded idle: give up (and stop the other roles) when nothing became ready for the wait limit.
+        if ((++spins & 63u) == 0) {
+          if (*abort_flag) break;
+          const uint64_t now = global_timer_ns();
+          if (spins == 64) {
+            t_idle = now;
+          } else if (now - t_idle > lim) {
+            raise_status(NC_DEV_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
       }
       // Every copy this CTA started must land before the CTA exits (already true on the normal path).
-      mbar_wait(q_full, 0, lim, nullptr);
-      for (int j = max(0, issued - kStages); j < issued; ++j) {
-        mbar_wait(k_full + (j & 1), (j >> 1) & 1, lim, nullptr);
-        mbar_wait(v_full + (j & 1), (j >> 1) & 1, lim, nullptr);
+      for (int t = max(0, kt - kKStages); t < kt; ++t) mbar_wait(k_full + t % kKStages, (t / kKStages) & 1, lim, nullptr);
+      for (int t = max(0, vt - kVStages); t < vt; ++t) mbar_wait(v_full + t % kVStages, (t / kVStages) & 1, lim, nullptr);
+      for (int i2 = max(0, iq - 1); i2 < iq; ++i2) {
+        mbar_wait(q_full + 0, i2 & 1, lim, nullptr);
+        mbar_wait(q_full + 1, i2 & 1, lim, nullptr);
       }
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
-      const uint32_t aQ = smem_u32(sQ);
-      const uint32_t aK = smem_u32(sK);
-      const uint32_t aV = smem_u32(sV);
-      bool ok = mbar_wait(q_full, 0, lim, abort_flag);
-      tc_fence_after_sync();
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {  // S_j = Q K_j^T
-          const int st = j & 1;
-          if (!(ok = mbar_wait(k_full + st, (j >> 1) & 1, lim, abort_flag))) break;
-          tc_fence_after_sync();
-          const uint32_t dS = tbase + kColS + st * 128;
+    } else if (warp == kMmaWarp || warp == kMmaWarpB) {
+      // ---------------------------------------------------------------- MMA issuer of Q tile x
+      // The whole warp walks the schedule and waits together (converged); lane 0 issues the MMAs and commits.
+      // Every shared-memory descriptor is built once; a K step of an MMA only adds a constant to the start-address
+      // field (addresses stay below 256 KB, so the 14-bit field never carries).
+      const int x = warp == kMmaWarp ? 0 : 1;
+      const bool leader = lane == 0;
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      // Tiles are 32 KB apart: the descriptor of buffer i is the one of buffer 0 plus i * (32 KB >> 4).
+      constexpr uint64_t kTileDesc = kTileBytes >> 4;
+      const uint64_t dq = sdesc_sw128(aQ, 16, 1024) + x * kTileDesc, dk0 = sdesc_sw128(aK, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(aV, kHalfBytes, 1024);
+      const uint32_t tS = tbase + kColS + x * 128, tO = tbase + kColO + x * 128;
+      auto issue_s = [&](int st) {  // S_X = Q_X K^T (K from stage st)
+        if (leader) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            umma_ss(dS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + st * kTileBytes + off, 16, 1024),
-                    kIdescQK, kk > 0 ? 1u : 0u);
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+            umma_ss(tS, dq + off, dk0 + st * kTileDesc + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
-          umma_commit(s_full + st);
+          umma_commit(s_full + x);
         }
-        if (j > 0) {  // O += P_{j-1} V_{j-1}
-          const int i = j - 1;
-          const int st = i & 1;
-          if (!(ok = mbar_wait(p_full + st, (i >> 1) & 1, lim, abort_flag))) break;
-          if (!(ok = mbar_wait(v_full + st, (i >> 1) & 1, lim, abort_flag))) break;
-          tc_fence_after_sync();
+        __syncwarp();
+      };
+      auto issue_pv = [&](int st, uint32_t acc0) {  // O_X (+)= P_X V (V from stage st)
+        if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            umma_ts(tbase + kColO, tbase + kColS + st * 128 + kk * 8,
-                    sdesc_sw128(aV + st * kTileBytes + kk * 2048, kHalfBytes, 1024), kIdescPV,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(o_done);
-          umma_commit(kv_empty + st);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tO, tS + kk * 8, dv0 + st * kTileDesc + static_cast<uint64_t>((kk * 2048) >> 4), kIdescPV,
+                    kk > 0 ? 1u : acc0);
+          umma_commit(o_done + x);
         }
+        __syncwarp();
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (leader) umma_commit(bar);
+        __syncwarp();
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, lim, abort_flag));
+      };
+      int kv = 0;    // KV tiles of the item sequence passed so far (ring positions)
+      int ns = 0;    // S / P.V products of Q tile x so far (phase of s_full / p_full / o_done)
+      int nit = 0;   // items in which Q tile x was active (phase of o_free)
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!(ok = wait(sched_full + slot, (k >> 1) & 1))) break;
+        const int item = sched[slot];
+        __syncwarp();
+        if (leader) mbar_arrive(sched_empty + slot);
+        if (item < 0) break;
+        const Item it = decode_item(p, item);
+        const QRange q = x == 0 ? it.qa : it.qb;
+        const int lo_x = q.n > 0 ? q.lo : INT_MAX, hi_x = q.n > 0 ? q.hi : INT_MIN;
+        // Both issuers wait for every Q, K and V buffer of the item to land -- also the ones their own tile does not
+        // use -- before releasing it: the release barriers count one commit from each issuer per fill, and an
+        // issuer that ran ahead would otherwise commit twice within one fill.
+        if (!(ok = wait(q_full + x, k & 1))) break;
+        if (!(ok = wait(k_full + kv % kKStages, (kv / kKStages) & 1))) break;
+        if (lo_x == it.lo) {
+          tc_fence_after_sync();
+          issue_s(kv % kKStages);
+        }
+        commit(k_empty + kv % kKStages);
+        for (int j = it.lo; ok && j <= it.hi; ++j, ++kv) {
+          const int vst = kv % kVStages, kst1 = (kv + 1) % kKStages;
+          if (!(ok = wait(v_full + vst, (kv / kVStages) & 1))) break;
+          if (j >= lo_x && j <= hi_x) {  // O_X += P_X V_j
+            if (j == lo_x && nit > 0 && !(ok = wait(o_free + x, (nit - 1) & 1))) break;
+            if (!(ok = wait(p_full + x, ns & 1))) break;
+            tc_fence_after_sync();
+            issue_pv(vst, j > lo_x ? 1u : 0u);
+            ++ns;
+          }
+          commit(v_empty + vst);
+          if (j < it.hi) {
+            if (!(ok = wait(k_full + kst1, ((kv + 1) / kKStages) & 1))) break;
+            if (j + 1 >= lo_x && j + 1 <= hi_x) {  // S_X = Q_X K_{j+1}^T
+              tc_fence_after_sync();
+              issue_s(kst1);
+            }
+            commit(k_empty + kst1);
+          }
+        }
+        if (!ok) break;
+        commit(q_empty);
+        nit += q.n > 0 ? 1 : 0;
       }
-      umma_commit(mma_final);  // all issued MMAs complete before TMEM is released
-      mbar_wait(mma_final, 0, lim, nullptr);
+      if (leader) umma_commit(mma_final + x);  // all issued MMAs complete before TMEM is released
+      __syncwarp();
+      mbar_wait(mma_final + x, 0, lim, nullptr);
     }
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
-    const int r = threadIdx.x;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const int tpos = r / p.G;
-    const int jh = r - tpos * p.G;
-    const int t = t0 + tpos;
-    const bool row_ok = (r < rows_used) && (t < p.T);
+    // ------------------------------------------------------------------ softmax + epilogue (warps 0-7)
+    warpgroup_reg_inc<kRegsSoftmax>();
+    const int r = threadIdx.x & 127;   // row of the Q tiles = TMEM lane
+    const int h = warp >> 2;           // column half: columns [64 h, 64 h + 64) of S and O
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
-    const uint32_t tO = tbase + lane_base + kColO;
-    float m = -INFINITY;  // running maximum of the raw scores of this row
-    float l = 0.f;        // running softmax denominator (relative to m)
+    const uint64_t sl2x2 = f32x2(sl2, sl2);
+    const uint64_t nbx2 = f32x2(-kScoreBound * sl2, -kScoreBound * sl2);
+    const int tpos = r / p.G;
+    constexpr uint32_t kBarAll = 1;    // named barrier of the 256 softmax threads
+    int ns[2] = {0, 0};   // S tiles of Q tile X consumed so far (all items)
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      ok = mbar_wait(s_full + st, (j >> 1) & 1, lim, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after_sync();
-      const uint32_t tS = tbase + lane_base + kColS + st * 128;
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tS + c4 * 32, sv[c4]);
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) tmem_ld_wait(sv[c4]);
-
-      const int s0 = (kt0 + j) * kBlockN;
-      const bool full_tile = (s0 + kBlockN - 1 <= t0) && (p.window < 0 || t_last - s0 <= p.window);
-      float mt = -INFINITY;
-      if (full_tile) {
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mt = fmaxf(mt, __uint_as_float(sv[c4][c]));
-      } else {
-        const int hi_c = t - s0;                                        // key index <= t
-        const int lo_c = p.window < 0 ? INT_MIN : t - s0 - p.window;  // t - key <= window
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int col = c4 * 32 + c;
-            float x = __uint_as_float(sv[c4][c]);
-            if (col > hi_c || col < lo_c) x = -INFINITY;
-            sv[c4][c] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
-          }
-      }
-      const float m_new = fmaxf(m, mt);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // a row with nothing visible yet keeps P = 0
-      const float nms = -m_use * sl2;
-      const float corr = ex2_approx((m - m_use) * sl2);           // 0 on the first visible tile
-      float rs = 0.f;
-      uint32_t pk[4][16];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c4][2 * c]), sl2, nms));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c4][2 * c + 1]), sl2, nms));
-          rs += p0 + p1;
-          pk[c4][c] = pack_bf16x2(p0, p1);
-        }
-      l = fmaf(l, corr, rs);
-      if (j > 0) {
-        // O holds the sum over tiles < j once the previous P.V has completed; rescale it to the new maximum.
-        ok = mbar_wait(o_done, (j - 1) & 1, lim, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, corr < 1.0f)) {
-#pragma unroll 1
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c4 * 32, ov);
-            tmem_ld_wait(ov);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * corr);
-            tmem_st32(tO + c4 * 32, ov);
-          }
-        }
-      }
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) tmem_st16(tS + c4 * 16, pk[c4]);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(p_full + st);
-      m = m_new;
-    }
-    if (ok) {
-      ok = mbar_wait(o_done, (n_kv - 1) & 1, lim, abort_flag);
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      ok = mbar_wait(sched_full + slot, (k >> 1) & 1, lim, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after_sync();
-      const float inv_l = 1.f / l;
-      uint4* dst = reinterpret_cast<uint4*>(
-          p.out + ((static_cast<size_t>(b) * p.T + (row_ok ? t : 0)) * p.Hq + g * p.G + jh) * kD);
-#pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c4 * 32, ov);
-        tmem_ld_wait(ov);
-        if (row_ok) {
+      if (!named_bar_and(kBarAll, 2 * kSoftThreads, ok)) break;
+      const int item = sched[slot];
+      named_bar_sync(kBarAll, 2 * kSoftThreads);
+      if (threadIdx.x == 0) mbar_arrive(sched_empty + slot);
+      if (item < 0) break;
+      const Item it = decode_item(p, item);
+      float l[2] = {0.f, 0.f};  // this half's running softmax denominator (relative to kScoreBound)
+      // Failure discipline: a failed wait only sets `fail`; every warp runs the same loop trip counts and reaches
+      // every barrier of the 256 softmax threads, each barrier ANDs the threads' status, and the warps leave the
+      // loops together, right after a barrier, when any of them failed.
+      bool fail = false;
+      for (int j = it.lo; ok && j <= it.hi; ++j) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint32_t q4[4];
+        for (int x = 0; x < 2; ++x) {
+          const QRange q = x == 0 ? it.qa : it.qb;
+          if (q.n == 0 || j < q.lo || j > q.hi) continue;
+          const uint32_t tS = tbase + lane_base + kColS + x * 128;
+          const int t = q.t0 + tpos;
+          if (!fail) fail = !mbar_wait(s_full + x, ns[x] & 1, lim, abort_flag);
+          fail = !__all_sync(0xffffffffu, !fail);
+          if (fail) continue;  // nothing more this round; the barrier after the rounds decides for everyone
+          tc_fence_after_sync();
+          uint32_t sv[2][32];
+          tmem_ld32(tS + 64 * h, sv[0]);
+          tmem_ld32(tS + 64 * h + 32, sv[1]);
+          tmem_ld_wait(sv[0]);
+          tmem_ld_wait(sv[1]);
+          const int s0 = j * kBlockN + 64 * h;  // key of this thread's first column
+          const bool full_tile = (j * kBlockN + kBlockN - 1 <= q.t0) &&
+                                 (p.window < 0 || q.t_last - j * kBlockN <= p.window);
+          if (!full_tile) {
+            const int hi_c = t - s0;                                        // key index <= t
+            const int lo_c = p.window < 0 ? INT_MIN : t - s0 - p.window;  // t - key <= window
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              q4[e] = pack_bf16x2(__uint_as_float(ov[8 * w + 2 * e]) * inv_l,
-                                  __uint_as_float(ov[8 * w + 2 * e + 1]) * inv_l);
-            dst[c4 * 4 + w] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+            for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int col = c2 * 32 + c;
+                if (col > hi_c || col < lo_c) sv[c2][c] = __float_as_uint(-INFINITY);
+              }
           }
+          // P = 2^((s - kScoreBound) sl2): exponents in [-33, 0], rounded to bf16, written over this half's part
+          // of the S row (keys [64 h, 64 h + 64) -> packed P columns [32 h, 32 h + 32)).  Pairs of columns go
+          // through packed fp32 instructions; all 32 pairs are computed before the two TMEM stores (which the
+          // compiler cannot move code across) so that the exponentials of the whole half row interleave.
+          uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial row sums (+0.0f in both lanes)
+          uint32_t pk[2][16];
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              float a0, a1;
+              f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c2][2 * c]), __uint_as_float(sv[c2][2 * c + 1])),
+                                    sl2x2, nbx2),
+                          a0, a1);
+              const uint32_t pp = pack_bf16x2(ex2_approx(a0), ex2_approx(a1));
+              pk[c2][c] = pp;
+              // the row sum adds the bf16 values the P.V product uses, so that O / l weighs every key exactly as
+              // the product does (a row with one visible key returns that key's value exactly)
+              rs2[c & 3] = add_f32x2(rs2[c & 3], f32x2(bf16_lo(pp), bf16_hi(pp)));
+            }
+          }
+          tmem_st16(tS + 32 * h, pk[0]);
+          tmem_st16(tS + 32 * h + 16, pk[1]);
+          float rsum = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float lo, hi;
+            f32x2_split(rs2[i], lo, hi);
+            rsum += lo + hi;
+          }
+          l[x] += rsum;
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(p_full + x);
+          ++ns[x];
+        }
+      }
+      // All 256 threads agree on the item's outcome before the epilogues use the exchange area.
+      if (!named_bar_and(kBarAll, 2 * kSoftThreads, ok && !fail)) break;
+      // ---- epilogues: O / l once the last P.V of each Q tile has completed
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const QRange q = x == 0 ? it.qa : it.qb;
+        if (q.n == 0) continue;
+        const uint32_t tO = tbase + lane_base + kColO + x * 128;
+        const bool row_in_box = r < p.G * p.P;  // rows past G * P belong to no query
+        fail = !mbar_wait(o_done + x, (ns[x] - 1) & 1, lim, abort_flag);
+        fail = !__all_sync(0xffffffffu, !fail);
+        float* lx = xch;  // [2 halves][128] row sums
+        if (!fail) lx[h * 128 + r] = l[x];
+        // the staging tile is free once the previous tile's TMA store has read it
+        if (threadIdx.x == 0) bulk_wait_read_all();
+        if (!named_bar_and(kBarAll, 2 * kSoftThreads, !fail)) { ok = false; break; }
+        const float inv_l = 1.f / (lx[r] + lx[128 + r]);
+        tc_fence_after_sync();
+        // O / l in bf16 into the staging tile: this thread's 64 columns are one 128-byte row of half h, laid out
+        // with the 128-byte swizzle of the output map (16-byte chunk c of row r at chunk position c ^ (r % 8)).
+        uint8_t* srow = sO + h * kHalfBytes + r * 128;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t ov[32];
+          tmem_ld32(tO + 64 * h + 32 * c2, ov);
+          tmem_ld_wait(ov);
+          if (row_in_box) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint32_t q4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                q4[e] = pack_bf16x2(__uint_as_float(ov[8 * w + 2 * e]) * inv_l,
+                                    __uint_as_float(ov[8 * w + 2 * e + 1]) * inv_l);
+              const int c = c2 * 4 + w;
+              *reinterpret_cast<uint4*>(srow + ((c ^ (r & 7)) << 4)) = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+            }
+          }
+        }
+        fence_proxy_async_smem();  // the generic-proxy writes above become visible to the TMA store
+        tc_fence_before_sync();
+        mbar_arrive(o_free + x);  // the MMA may start the next item's P.V into O_X
+        named_bar_sync(kBarAll, 2 * kSoftThreads);  // staging tile written; the row-sum area is free again
+        if (threadIdx.x == 0) {  // rows past T fall outside the tensor and are not written
+          tma_store_4d(&tmO, sO, 0, it.g * p.G, q.t0, it.b);
+          tma_store_4d(&tmO, sO + kHalfBytes, 64, it.g * p.G, q.t0, it.b);
+          bulk_commit_group();
         }
       }
     }
   }
 
   // ------------------------------------------------------------------ teardown
+  if (threadIdx.x == 0) bulk_wait_all();  // the output stores have read (and written) everything
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) {

@@ -102,13 +102,26 @@ void set_smem_attr_once(F* kernel, int bytes, int slot) {
 nc_status launch_status() { return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA; }
 
 nc_status launch_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
-                          const RopeTable& tab, cudaStream_t stream) {
+                          const RopeTable& tab, unsigned* zero_word, cudaStream_t stream) {
   const int BT = B * T;
   const int blocks = (BT + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
   nc::qk_prologue_kernel<<<blocks, nc::kPrologueThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(qn),
-      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab);
+      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, zero_word);
   return launch_status();
+}
+
+// Resident CTAs per device for the persistent kernels: one per SM.
+int sm_count() {
+  static int cached[16] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 // ---- library-held workspaces for the entry points without a workspace argument -------------------------------
@@ -175,15 +188,8 @@ void launch_decode_g(int grid, const CUtensorMap& mk, const CUtensorMap& mv, con
 
 // Resident CTAs of the decode kernel on the current device: one per SM, at most kMaxParts.
 int decode_grid() {
-  static int cached[16] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 0;
-    cached[dev] = n < nc::dec::kMaxParts ? n : nc::dec::kMaxParts;
-  }
-  return cached[dev];
+  const int n = sm_count();
+  return n < nc::dec::kMaxParts ? n : nc::dec::kMaxParts;
 }
 
 nc_status check_decode_args(const void* q, const void* kcache, const void* vcache, const int* cache_lens,
@@ -223,7 +229,7 @@ nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, 
   if (!rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
   const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
   if (st != NC_OK) return st;
-  return launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), stream);
+  return launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), nullptr, stream);
 }
 
 nc_status nc_attn_fwd_ws(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
@@ -246,21 +252,25 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   if (G > 128) return NC_ERR_UNSUPPORTED;
   const int P = 128 / G;
   const int n_qtiles = (T + P - 1) / P;
-  if (n_qtiles > 65535 || static_cast<long long>(B) * Hkv > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
+  const int n_pairs = (n_qtiles + 1) / 2;
+  if (static_cast<long long>(B) * Hkv * n_pairs > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
   const size_t need = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return NC_ERR_WORKSPACE;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* qn = ws;
   void* kn = ws + 2ull * static_cast<size_t>(B) * T * Hq * D;
+  unsigned* item_ctr = reinterpret_cast<unsigned*>(ws + 2ull * static_cast<size_t>(B) * T * (Hq + Hkv) * D);
+  const int n_sm = sm_count();
+  if (n_sm < 1) return NC_ERR_CUDA;
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map_4d(&mq, qn, 128, Hq, T, B, 64, G, P, 1) || !make_map_4d(&mk, kn, 128, Hkv, T, B, 64, 1, 128, 1) ||
-      !make_map_4d(&mv, v, 128, Hkv, T, B, 64, 1, 128, 1))
+      !make_map_4d(&mv, v, 128, Hkv, T, B, 64, 1, 128, 1) || !make_map_4d(&mo, out, 128, Hq, T, B, 64, G, P, 1))
     return NC_ERR_CUDA;
 
   if (k1_begin != nullptr && cudaEventRecord(k1_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
-  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), stream);
+  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), item_ctr, stream);
   if (st != NC_OK) return st;
   if (k2_begin != nullptr && cudaEventRecord(k2_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
 
@@ -272,13 +282,15 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   prm.Hkv = Hkv;
   prm.G = G;
   prm.P = P;
-  prm.n_qtiles = n_qtiles;
+  prm.n_pairs = n_pairs;
+  prm.n_items = B * Hkv * n_pairs;
+  prm.item_ctr = item_ctr;
   prm.window = window;
   prm.scale_log2 = scale_log2_for_d128();
   prm.wait_limit_ns = kWaitLimitNs;
   set_smem_attr_once(nc::fwd::attn_fwd_kernel, nc::fwd::kSmemBytes, 0);
-  dim3 grid(B * Hkv, n_qtiles);
-  nc::fwd::attn_fwd_kernel<<<grid, nc::fwd::kThreads, nc::fwd::kSmemBytes, stream>>>(mq, mk, mv, prm);
+  const int grid = std::min(n_sm, prm.n_items);
+  nc::fwd::attn_fwd_kernel<<<grid, nc::fwd::kThreads, nc::fwd::kSmemBytes, stream>>>(mq, mk, mv, mo, prm);
   st = launch_status();
   if (st == NC_OK && k2_end != nullptr && cudaEventRecord(k2_end, stream) != cudaSuccess) return NC_ERR_CUDA;
   return st;
@@ -401,6 +413,7 @@ nc_status nc_attn_get_device_status(cudaStream_t stream, int clear) {
   }
   if (v & nc::NC_DEV_TIMEOUT) return NC_ERR_DEVICE_TIMEOUT;
   if (v & nc::NC_DEV_BAD_CACHE_LEN) return NC_ERR_DEVICE_BAD_INPUT;
+  if (v & nc::NC_DEV_SMEM_BASE) return NC_ERR_UNSUPPORTED;
   return NC_OK;
 }
 

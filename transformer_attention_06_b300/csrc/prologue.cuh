@@ -81,7 +81,9 @@ constexpr int kPrologueTokensPerBlock = kPrologueThreads / 8;
 __global__ void __launch_bounds__(kPrologueThreads)
     qk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                        __nv_bfloat16* __restrict__ qn, __nv_bfloat16* __restrict__ kn, int BT, int T, int Hq,
-                       int Hkv, const __grid_constant__ RopeTable tab) {
+                       int Hkv, const __grid_constant__ RopeTable tab, unsigned* zero_word) {
+  // The attention kernel that follows in stream order takes its work items from this counter.
+  if (zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0u;
   const int tok = blockIdx.x * kPrologueTokensPerBlock + (threadIdx.x >> 3);
   const int kq = threadIdx.x & 7;
   if (tok >= BT) return;  // whole 8-lane groups leave together
