@@ -229,6 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
+  // Everything above ran concurrently with the tail of the prologue kernel; qn, kn and the work counter are read
+  // only after it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t q_bytes = 2u * 128u * static_cast<uint32_t>(p.G * p.P);  // one Q tile (box {64, G, P, 1} x 2)
   if (warp >= 8) {
     warpgroup_reg_dec<kRegsOther>();
@@ -474,15 +477,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool full_tile = (j * kBlockN + kBlockN - 1 <= q.t0) &&
                                  (p.window < 0 || q.t_last - j * kBlockN <= p.window);
           if (!full_tile) {
-            const int hi_c = t - s0;                                        // key index <= t
-            const int lo_c = p.window < 0 ? INT_MIN : t - s0 - p.window;  // t - key <= window
+            // visible columns form the interval [lo_c, hi_c]: key <= t, and t - key <= window
+            const int hi_c = t - s0;
+            const int lo_c = p.window < 0 ? -64 : hi_c - p.window;
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2)
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int a = lo_c - 32 * c2, b = hi_c - 32 * c2;  // the interval within these 32 columns
+              const uint32_t m_hi = b >= 31 ? ~0u : (b < 0 ? 0u : (2u << b) - 1u);
+              const uint32_t m_lo = a <= 0 ? ~0u : (a > 31 ? 0u : ~((1u << a) - 1u));
+              const uint32_t vis = m_hi & m_lo;
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const int col = c2 * 32 + c;
-                if (col > hi_c || col < lo_c) sv[c2][c] = __float_as_uint(-INFINITY);
-              }
+              for (int c = 0; c < 32; ++c)
+                if (!((vis >> c) & 1u)) sv[c2][c] = __float_as_uint(-INFINITY);
+            }
           }
           // P = 2^((s - kScoreBound) sl2): exponents in [-33, 0], rounded to bf16, written over this half's part
           // of the S row (keys [64 h, 64 h + 64) -> packed P columns [32 h, 32 h + 32)).  Pairs of columns go

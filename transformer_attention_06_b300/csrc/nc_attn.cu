@@ -290,7 +290,19 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   prm.wait_limit_ns = kWaitLimitNs;
   set_smem_attr_once(nc::fwd::attn_fwd_kernel, nc::fwd::kSmemBytes, 0);
   const int grid = std::min(n_sm, prm.n_items);
-  nc::fwd::attn_fwd_kernel<<<grid, nc::fwd::kThreads, nc::fwd::kSmemBytes, stream>>>(mq, mk, mv, mo, prm);
+  // Programmatic dependent launch: the CTAs may start (and set up barriers and TMEM) while the prologue drains;
+  // they wait on the prologue grid (griddepcontrol.wait) before touching anything it writes.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(nc::fwd::kThreads);
+  cfg.dynamicSmemBytes = nc::fwd::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, nc::fwd::attn_fwd_kernel, mq, mk, mv, mo, prm) != cudaSuccess) return launch_status();
   st = launch_status();
   if (st == NC_OK && k2_end != nullptr && cudaEventRecord(k2_end, stream) != cudaSuccess) return NC_ERR_CUDA;
   return st;

@@ -82,7 +82,10 @@ __global__ void __launch_bounds__(kPrologueThreads)
     qk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                        __nv_bfloat16* __restrict__ qn, __nv_bfloat16* __restrict__ kn, int BT, int T, int Hq,
                        int Hkv, const __grid_constant__ RopeTable tab, unsigned* zero_word) {
-  // The attention kernel that follows in stream order takes its work items from this counter.
+  // The attention kernel that follows in stream order may be scheduled now; it waits for this grid to complete
+  // before reading anything written here.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The attention kernel takes its work items from this counter.
   if (zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0u;
   const int tok = blockIdx.x * kPrologueTokensPerBlock + (threadIdx.x >> 3);
   const int kq = threadIdx.x & 7;
