@@ -102,12 +102,12 @@ void set_smem_attr_once(F* kernel, int bytes, int slot) {
 nc_status launch_status() { return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA; }
 
 nc_status launch_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
-                          const RopeTable& tab, unsigned* zero_word, cudaStream_t stream) {
+                          const RopeTable& tab, float q_scale, unsigned* zero_word, cudaStream_t stream) {
   const int BT = B * T;
   const int blocks = (BT + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
   nc::qk_prologue_kernel<<<blocks, nc::kPrologueThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(qn),
-      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, zero_word);
+      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, q_scale, zero_word);
   return launch_status();
 }
 
@@ -229,7 +229,7 @@ nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, 
   if (!rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
   const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
   if (st != NC_OK) return st;
-  return launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), nullptr, stream);
+  return launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), 1.0f, nullptr, stream);
 }
 
 nc_status nc_attn_fwd_ws(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
@@ -270,7 +270,8 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
     return NC_ERR_CUDA;
 
   if (k1_begin != nullptr && cudaEventRecord(k1_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
-  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), item_ctr, stream);
+  // qn leaves the prologue multiplied by log2(e) / sqrt(D): the attention kernel's scores are then base-2 logits.
+  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), scale_log2_for_d128(), item_ctr, stream);
   if (st != NC_OK) return st;
   if (k2_begin != nullptr && cudaEventRecord(k2_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
 
@@ -286,7 +287,6 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   prm.n_items = B * Hkv * n_pairs;
   prm.item_ctr = item_ctr;
   prm.window = window;
-  prm.scale_log2 = scale_log2_for_d128();
   prm.wait_limit_ns = kWaitLimitNs;
   set_smem_attr_once(nc::fwd::attn_fwd_kernel, nc::fwd::kSmemBytes, 0);
   const int grid = std::min(n_sm, prm.n_items);

@@ -7,7 +7,8 @@
 // Memory-bound: it reads q and k once and writes qn and kn once (2 * 2 * B*T*(Hq+Hkv)*128 bytes).  Mapping: an
 // 8-lane group per token; lane kq of the group owns pairs [8kq, 8kq+8), i.e. two 16-byte slices of every head
 // vector of the token, so the cos/sin of the token are computed once and reused across all Hq + Hkv heads.  The
-// sum of squares is reduced across the group with three xor-shuffles.
+// sum of squares is reduced across the group with three xor-shuffles.  The normalised q vectors may be multiplied
+// by a constant on the way out (the attention kernel takes the softmax scale log2(e) / sqrt(D) this way).
 #pragma once
 
 #include "common.cuh"
@@ -15,10 +16,10 @@
 namespace nc {
 
 // Rotates the 8 pairs held in (lo, hi) -- elements [8kq, 8kq+8) and [64+8kq, 64+8kq+8) of a 128-wide head
-// vector -- and normalises by the RMS of the whole vector (reduced over the 8-lane group `gmask`).
+// vector -- and normalises by the RMS of the whole vector (reduced over the 8-lane group `gmask`), times `scale`.
 __device__ __forceinline__ void rope_norm_slices(const uint4& lo, const uint4& hi, const float (&c)[8],
-                                                 const float (&s)[8], unsigned gmask, float (&y1)[8],
-                                                 float (&y2)[8]) {
+                                                 const float (&s)[8], unsigned gmask, float scale,
+                                                 float (&y1)[8], float (&y2)[8]) {
   const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w};
   const uint32_t b[4] = {hi.x, hi.y, hi.z, hi.w};
   float ss = 0.f;
@@ -34,7 +35,7 @@ __device__ __forceinline__ void rope_norm_slices(const uint4& lo, const uint4& h
   ss += __shfl_xor_sync(gmask, ss, 1);
   ss += __shfl_xor_sync(gmask, ss, 2);
   ss += __shfl_xor_sync(gmask, ss, 4);
-  const float inv = rsqrtf(ss * (1.0f / 128.0f) + kRmsEps);
+  const float inv = rsqrtf(ss * (1.0f / 128.0f) + kRmsEps) * scale;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     y1[i] *= inv;
@@ -51,7 +52,7 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&y)[8]) {
 // 16-byte loads per lane are in flight before any arithmetic.
 __device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst,
                                                 int H, int kq, const float (&c)[8], const float (&s)[8],
-                                                unsigned gmask) {
+                                                unsigned gmask, float scale) {
   const uint4* in = reinterpret_cast<const uint4*>(src);
   uint4* out = reinterpret_cast<uint4*>(dst);
   for (int h0 = 0; h0 < H; h0 += 4) {
@@ -67,7 +68,7 @@ __device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict_
     for (int u = 0; u < 4; ++u) {
       if (h0 + u < H) {
         float y1[8], y2[8];
-        rope_norm_slices(lo[u], hi[u], c, s, gmask, y1, y2);
+        rope_norm_slices(lo[u], hi[u], c, s, gmask, scale, y1, y2);
         out[(h0 + u) * 16 + kq] = pack8_bf16(y1);
         out[(h0 + u) * 16 + 8 + kq] = pack8_bf16(y2);
       }
@@ -81,7 +82,7 @@ constexpr int kPrologueTokensPerBlock = kPrologueThreads / 8;
 __global__ void __launch_bounds__(kPrologueThreads)
     qk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                        __nv_bfloat16* __restrict__ qn, __nv_bfloat16* __restrict__ kn, int BT, int T, int Hq,
-                       int Hkv, const __grid_constant__ RopeTable tab, unsigned* zero_word) {
+                       int Hkv, const __grid_constant__ RopeTable tab, float q_scale, unsigned* zero_word) {
   // The attention kernel that follows in stream order may be scheduled now; it waits for this grid to complete
   // before reading anything written here.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -96,9 +97,9 @@ __global__ void __launch_bounds__(kPrologueThreads)
 #pragma unroll
   for (int i = 0; i < 8; ++i) rope_cos_sin(pos, tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
   rope_norm_heads(q + static_cast<size_t>(tok) * Hq * 128, qn + static_cast<size_t>(tok) * Hq * 128, Hq, kq, c, s,
-                  gmask);
+                  gmask, q_scale);
   rope_norm_heads(k + static_cast<size_t>(tok) * Hkv * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq, c,
-                  s, gmask);
+                  s, gmask, 1.0f);
 }
 
 }  // namespace nc
