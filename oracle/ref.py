@@ -17,7 +17,7 @@ What is computed, and where the pages say so:
   (B, T, H, D), per-row int32 cache_seqlens, in-place append) and section 6 (SDPA decode case slices the KV
   window).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * RoPE pairs element i with element i + D/2 (half-split), frequency theta_i = base^(-2i/D), angle t*theta_i,
   and the rotation  y[i] = x[i] cos a + x[i+D/2] sin a,  y[i+D/2] = -x[i] sin a + x[i+D/2] cos a.
@@ -187,4 +187,44 @@ def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
             s = (keys[lo:L, g] @ qn[h]) * scale
             pr = _softmax_rows(s[None, :])[0]
             out[b, h] = pr @ vals[lo:L, g]
+    return out, kn_new
+
+
+def attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, window, rope_base=ROPE_BASE, eps=RMS_EPS):
+    """Chunked prefill against a KV cache -- Guide section 6 (the SDPA fallback's chunked / sliding-window
+    inference case: the chunk's queries attend to the cache plus the chunk) and section 7 "KV cache" (in-place
+    append at cache_seqlens).
+
+    q: [B, Tq, Hq, D] raw queries; k_new, v_new: [B, Tq, Hkv, D] raw keys and values of the chunk;
+    kcache, vcache: [B, Tcap, Hkv, D] with rows 0..p_b-1 already roped + normed; cache_lens: [B] integers p_b.
+
+    Returns (out [B, Tq, Hq, D] fp64, kn_new [B, Tq, Hkv, D] fp64).  Query t and key t of the chunk sit at
+    position p_b + t.  The keys of sequence b are its cache rows 0..p_b-1 as given followed by
+    norm(rope(k_new[b, t], p_b + t)), with the values vcache[b, :p_b] followed by v_new[b]; key position j is
+    visible to query position i under ``visible``.  A p_b outside [0, Tcap - Tq] gives zero rows (and a zero
+    kn_new) for that sequence.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Tq, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    Tcap = kcache.shape[1]
+    G = Hq // Hkv
+    scale = 1.0 / np.sqrt(D)
+    out = np.zeros((B, Tq, Hq, D), dtype=np.float64)
+    kn_new = np.zeros((B, Tq, Hkv, D), dtype=np.float64)
+    for b in range(B):
+        p = int(cache_lens[b])
+        if p < 0 or p + Tq > Tcap:
+            continue
+        pos = p + np.arange(Tq)
+        qn = qk_prologue(q[b][None], pos[None], rope_base, eps)[0]                                   # [Tq, Hq, D]
+        kn_new[b] = qk_prologue(np.asarray(k_new[b], dtype=np.float64)[None], pos[None], rope_base, eps)[0]
+        keys = np.concatenate([np.asarray(kcache[b, :p], dtype=np.float64), kn_new[b]], axis=0)      # [p+Tq, Hkv, D]
+        vals = np.concatenate([np.asarray(vcache[b, :p], dtype=np.float64),
+                               np.asarray(v_new[b], dtype=np.float64)], axis=0)
+        mask = visible(pos[:, None], np.arange(p + Tq)[None, :], window)
+        for h in range(Hq):
+            g = h // G
+            s = np.where(mask, (qn[:, h] @ keys[:, g].T) * scale, -np.inf)
+            out[b, :, h] = _softmax_rows(s) @ vals[:, g]
     return out, kn_new

@@ -7,7 +7,8 @@ workloads.  Recipe (the same bf16 tensors go to both sides):
 * ``torch.randn(shape, dtype=float32, generator=g)`` in the order q, k, v (prefill) or
   k-cache, v-cache, cache lengths, q, [k_new, v_new] (decode);
 * each draw is rounded to bfloat16 (round-to-nearest-even) with ``.to(torch.bfloat16)``;
-* decode cache lengths: ``torch.randint(lo, hi + 1, (B,), generator=g)`` (uniform on [lo, hi]).
+* decode cache lengths: ``torch.randint(lo, hi + 1, (B,), generator=g)`` (uniform on [lo, hi]);
+* chunked prefill: k-cache, v-cache, q, k_new, v_new in that order; the cache lengths are given, not drawn.
 
 Values are N(0, 1), the distribution the nanochat workloads below are quoted with.  Shapes follow nanochat
 configurations (depth 12 gives model dim 768 = 6 heads of 128; GQA and long-context variants).
@@ -55,6 +56,24 @@ FWD_WORKLOADS = (TINY, DEPTH12, GQA, LONG)
 DECODE = DecodeWorkload("decode_b64_hq12_hkv4_w2048", 64, 12, 4, 128, 4097, 2048, 1, 4096)
 
 
+@dataclass(frozen=True)
+class ChunkWorkload:
+    name: str
+    B: int
+    Tq: int
+    Hq: int
+    Hkv: int
+    D: int
+    Tcap: int
+    p0: int          # cache length of every sequence when the chunk arrives
+    windows: tuple
+
+
+# Chunked prefill: the last 512 tokens of a 2048-token depth-12 context appended to a cache holding the first
+# 1536, once with a short-window layer's window and once with the full-context layer's.
+CHUNK = ChunkWorkload("chunk_depth12_b4_tq512_p1536", 4, 512, 6, 6, 128, 2048, 1536, (1024, 2048))
+
+
 def _randn(shape, g):
     return torch.randn(shape, dtype=torch.float32, generator=g).to(torch.bfloat16)
 
@@ -84,3 +103,15 @@ def decode_inputs(B, Hq, Hkv, D, Tcap, len_lo, len_hi, seed=0, with_new=False):
         k_new = _randn((B, Hkv, D), gen)
         v_new = _randn((B, Hkv, D), gen)
     return dict(kcache=kcache, vcache=vcache, cache_lens=cache_lens, q=q, k_new=k_new, v_new=v_new)
+
+
+def chunk_inputs(B, Tq, Hq, Hkv, D, Tcap, seed=0):
+    """Chunked-prefill inputs as bf16 CPU tensors: kcache, vcache [B,Tcap,Hkv,D] (taken as already roped and
+    normed, like the decode cache), q [B,Tq,Hq,D], k_new, v_new [B,Tq,Hkv,D]."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    kcache = _randn((B, Tcap, Hkv, D), gen)
+    vcache = _randn((B, Tcap, Hkv, D), gen)
+    q = _randn((B, Tq, Hq, D), gen)
+    k_new = _randn((B, Tq, Hkv, D), gen)
+    v_new = _randn((B, Tq, Hkv, D), gen)
+    return dict(kcache=kcache, vcache=vcache, q=q, k_new=k_new, v_new=v_new)
