@@ -85,6 +85,40 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
 nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
                               int D, float rope_base, cudaStream_t stream);
 
+/* ---- Chunked prefill against a KV cache ------------------------------------------------------------------------
+ * ("nanochat Admin & Developer Guide", section 6: the SDPA fallback's third case, chunked / sliding-window
+ * inference, where the queries of a chunk attend to the cache plus the chunk; section 7 "KV cache": FA3 layout
+ * (B, T, H, D), per-row cache_seqlens, in-place append.)  Tq new tokens per sequence b, at positions
+ * p_b + t (t < Tq) with p_b = cache_lens[b].
+ *   q:[B,Tq,Hq,D]                 raw queries of the chunk (roped at p_b + t and normed inside the call)
+ *   k_new,v_new:[B,Tq,Hkv,D]      raw keys and values of the chunk; norm(rope(k_new[b,t], p_b + t)) and v_new[b,t]
+ *                                 are written to cache row p_b + t (in place)
+ *   kcache,vcache:[B,Tcap,Hkv,D]  rows 0..p_b-1 are used as given (already roped and normed); rows at or past
+ *                                 p_b + Tq are never read into the result (they may hold anything)
+ *   cache_lens: device int32[B]   read only; the caller advances it by Tq after the call
+ *   out:[B,Tq,Hq,D]
+ * Query t of sequence b sees cache rows j <= p_b + t with p_b + t - j <= window (window -1 = all); the result
+ * equals rows p_b .. p_b+Tq-1 of nc_attn_fwd over the whole sequence.  A p_b outside [0, Tcap - Tq] gives zero
+ * output rows for that sequence, leaves its cache untouched and sets NC_ERR_DEVICE_BAD_INPUT in the device status
+ * word.  Requires Tcap >= Tq and Hq % Hkv == 0, D == 128.
+ *
+ * nc_attn_prefill_chunk_ws takes a caller-owned, 16-byte aligned device workspace of at least
+ * nc_attn_prefill_chunk_workspace_bytes(...) bytes (normed queries, a zero-padded copy of each sequence's last V
+ * tile, a counter); it needs no initialisation.  nc_attn_prefill_chunk uses a workspace owned by the library
+ * (same growth and stream rules as nc_attn_fwd).  Two calls that share a workspace must not overlap on the GPU.
+ * The pages have no such entry point under this name; it is the chunked case of their attention call.
+ */
+size_t nc_attn_prefill_chunk_workspace_bytes(int B, int Tq, int Hq, int Hkv, int D);
+
+nc_status nc_attn_prefill_chunk_ws(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                                   const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D,
+                                   int Tcap, int window, float rope_base, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
+nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                                const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D, int Tcap,
+                                int window, float rope_base, cudaStream_t stream);
+
 /* ---- KV-cache single-token decode ------------------------------------------------------------------------------
  * One new query token per sequence b, at position p_b = cache_lens[b].
  *   q:[B,Hq,D]            raw query of the new token (roped at position p_b, then normed, inside the call)

@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nc_attn_fwd", "nc_attn_fwd_ws", "nc_attn_decode", "nc_attn_decode_ws", "nc_attn_status_string",
-              "nc_attn_get_device_status", "nc_attn_qk_prologue"):
+              "nc_attn_get_device_status", "nc_attn_qk_prologue", "nc_attn_prefill_chunk", "nc_attn_prefill_chunk_ws"):
         assert n in names
 
 
@@ -100,7 +100,37 @@ def test_decode_rejects_bad_arguments(nc):
     assert dec(nc, ws=P, wsb=need - 1) == WS
 
 
+def chunk(nc, q=P, kn=P, vn=P, kc=P, vc=P, lens=P, out=P, B=2, Tq=100, Hq=6, Hkv=2, D=128, Tcap=300, W=-1,
+          base=1e5, ws=None, wsb=0):
+    return nc.lib.nc_attn_prefill_chunk_ws(q, kn, vn, kc, vc, lens, out, B, Tq, Hq, Hkv, D, Tcap, W, base, ws, wsb,
+                                           None)
+
+
+def test_prefill_chunk_rejects_bad_arguments(nc):
+    E, U, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_UNSUPPORTED, nc.NC_ERR_WORKSPACE
+    assert chunk(nc, q=None) == E
+    assert chunk(nc, vn=None) == E
+    assert chunk(nc, lens=None) == E
+    assert chunk(nc, kc=PM) == E
+    assert chunk(nc, lens=ctypes.c_void_p(0x10002)) == E
+    assert chunk(nc, Tq=0) == E
+    assert chunk(nc, Tcap=99) == E               # the chunk does not fit the cache
+    assert chunk(nc, Hq=5, Hkv=2) == E
+    assert chunk(nc, W=-2) == E
+    assert chunk(nc, base=0.0) == E
+    assert chunk(nc, D=64) == U
+    assert chunk(nc, Tcap=1 << 24) == U          # cache positions must be exact in fp32
+    assert chunk(nc, Hq=256, Hkv=1) == U
+    assert chunk(nc) == WS
+    need = nc.nc_attn_prefill_chunk_workspace_bytes(2, 100, 6, 2)
+    assert chunk(nc, ws=P, wsb=need - 1) == WS
+    assert chunk(nc, ws=PM, wsb=need) == WS
+
+
 def test_workspace_sizes(nc):
+    # chunked prefill: qn of the chunk and one 128-row V tail copy per sequence, in bf16, plus a counter
+    assert nc.nc_attn_prefill_chunk_workspace_bytes(4, 512, 6, 6) >= 2 * 4 * 512 * 6 * 128 + 2 * 4 * 128 * 6 * 128
+    assert nc.nc_attn_prefill_chunk_workspace_bytes(4, 512, 6, 4) == 0
     # qn + kn in bf16 plus a small pad
     assert nc.nc_attn_fwd_workspace_bytes(4, 2048, 6, 6) >= 2 * 4 * 2048 * 12 * 128
     assert nc.nc_attn_fwd_workspace_bytes(0, 2048, 6, 6) == 0

@@ -2,13 +2,15 @@
 //
 // What it computes ("nanochat Admin & Developer Guide", sections 3 and 6): for query row (b, t, h) with kv head
 // g = h / G, out = softmax_j(qn . kn_j / sqrt(D)) . v_j over the visible keys j (j <= t, and t - j <= window when
-// window >= 0).  qn / kn are the roped + normed vectors written by K1.
+// window >= 0).  qn / kn are the roped + normed vectors written by K1.  With per-sequence offsets p0 (chunked
+// prefill against a KV cache, "nanochat Admin & Developer Guide" section 6, SDPA case 3), query t sits at
+// position p0 + t and the keys come from the cache: positions replace t in the band and the mask.
 //
 // Tiling.  A Q tile is 128 MMA rows: P = 128 / G consecutive query positions times the G query heads of kv head g
 // (row r = position r / G, head r % G), so every K/V tile brought in by TMA serves the whole GQA group.  A work item
-// is two consecutive Q tiles (A and B) of one (b, g): every K/V tile is loaded once for both.  Keys are processed
-// in tiles of 128; a Q tile only visits the key tiles that intersect its causal / window band, and only tiles that
-// straddle the band edge pay for the element mask.
+// is two consecutive Q tiles (A and B) of one (b, g): every K/V tile is loaded once for both (or a single tile, when
+// pairs would leave SMs without an item).  Keys are processed in tiles of 128; a Q tile only visits the key tiles
+// that intersect its causal / window band, and only tiles that straddle the band edge pay for the element mask.
 //
 // Persistent grid: one CTA per SM takes work items from a global counter (zeroed by the prologue kernel), the
 // latest (heaviest under a causal mask) Q tiles first, so the tail of the launch is made of the lightest items.
@@ -98,29 +100,37 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 struct Params {
   __nv_bfloat16* out;
   unsigned* item_ctr;                 // work-item counter, zero at launch (written by the prologue kernel)
+  // Position of query 0 of sequence b (chunked prefill against a cache: the cache length); null means 0.
+  const int* pos0;
   int B, T, Hq, Hkv, G, P, n_pairs, n_items, window;
+  int tiles_per_item;                 // 2 (Q tiles A and B share every K/V tile), or 1 when pairs would leave SMs idle
+  int Tk;                             // key rows per sequence that the K / V maps address (T, or the cache size)
   unsigned long long wait_limit_ns;
 };
 
-// Key-tile range of one Q tile: tiles [lo, hi] intersect its band; n = 0 when the tile lies past T.
+// Key-tile range of one Q tile: tiles [lo, hi] intersect its band; n = 0 when the tile lies past T.  Query rows
+// t0 .. t_last sit at positions a0 .. a_last (= p0 + t).
 struct QRange {
-  int t0, t_last, lo, hi, n;
+  int t0, t_last, a0, a_last, lo, hi, n;
 };
 
-__device__ __forceinline__ QRange q_range(const Params& p, int t0) {
+__device__ __forceinline__ QRange q_range(const Params& p, int t0, int p0) {
   QRange q;
   q.t0 = t0;
+  q.a0 = p0 + t0;
   if (t0 >= p.T) {
     q.t_last = t0 - 1;
+    q.a_last = q.a0 - 1;
     q.lo = 0;
     q.hi = -1;
     q.n = 0;
     return q;
   }
   q.t_last = min(t0 + p.P, p.T) - 1;
-  const int key_lo = p.window < 0 ? 0 : max(0, t0 - p.window);
+  q.a_last = p0 + q.t_last;
+  const int key_lo = p.window < 0 ? 0 : max(0, q.a0 - p.window);
   q.lo = key_lo / kBlockN;
-  q.hi = q.t_last / kBlockN;
+  q.hi = q.a_last / kBlockN;
   q.n = q.hi - q.lo + 1;
   return q;
 }
@@ -128,7 +138,9 @@ __device__ __forceinline__ QRange q_range(const Params& p, int t0) {
 struct Item {
   int b, g;
   QRange qa, qb;
-  int lo, hi;  // union of the two key-tile ranges
+  int lo, hi;   // union of the two key-tile ranges
+  int tail;     // key tile read from the zero-padded V tail copy (-1: none)
+  bool valid;   // false: the sequence's cache length is out of range; nothing is stored
 };
 
 __device__ __forceinline__ Item decode_item(const Params& p, int item) {
@@ -138,17 +150,22 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item) {
   const int bg = item - (item / bh) * bh;
   it.b = bg / p.Hkv;
   it.g = bg - it.b * p.Hkv;
-  it.qa = q_range(p, pair * 2 * p.P);
-  it.qb = q_range(p, pair * 2 * p.P + p.P);
+  const int pp = p.pos0 != nullptr ? __ldg(p.pos0 + it.b) : 0;
+  it.valid = pp >= 0 && pp <= p.Tk - p.T;
+  const int p0 = it.valid ? pp : 0;
+  // n_pairs counts the items of one (b, g); with one tile per item, tile B starts past T (empty)
+  it.qa = q_range(p, pair * p.tiles_per_item * p.P, p0);
+  it.qb = q_range(p, p.tiles_per_item == 2 ? pair * 2 * p.P + p.P : p.T, p0);
   it.lo = it.qa.lo;
   it.hi = it.qb.n > 0 ? max(it.qa.hi, it.qb.hi) : it.qa.hi;
+  it.tail = p.pos0 != nullptr ? (p0 + p.T - 1) / kBlockN : -1;
   return it;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVt,
+                    const __grid_constant__ CUtensorMap tmO, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem + kOffQ;
@@ -240,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmO);
+      if (p.pos0 != nullptr) tma_prefetch_desc(&tmVt);
       // Items fetched so far live in a 2-slot ring (the same slots the consumers read).  Three cursors walk the
       // item sequence: Q (item iq), K (item ik, tile jk), V (item iv, tile jv); kt / vt count the K / V tiles
       // loaded over all items (ring positions).
@@ -300,8 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = vt % kVStages;
             uint8_t* dv = sV + st * kTileBytes;
             mbar_arrive_expect_tx(v_full + st, kTileBytes);
-            tma_load_4d(dv, &tmV, v_full + st, 0, it.g, jv * kBlockN, it.b);
-            tma_load_4d(dv + kHalfBytes, &tmV, v_full + st, 64, it.g, jv * kBlockN, it.b);
+            // the tile holding the last key of a chunked prefill comes from its zero-padded copy: cache rows past
+            // the chunk may hold anything, and P = 0 times a NaN would still poison O
+            const bool from_tail = jv == it.tail;
+            const CUtensorMap* mv = from_tail ? &tmVt : &tmV;
+            const int row = from_tail ? 0 : jv * kBlockN;
+            tma_load_4d(dv, mv, v_full + st, 0, it.g, row, it.b);
+            tma_load_4d(dv + kHalfBytes, mv, v_full + st, 64, it.g, row, it.b);
             ++vt;
             if (++jv > it.hi) {
               ++iv;
@@ -459,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const QRange q = x == 0 ? it.qa : it.qb;
           if (q.n == 0 || j < q.lo || j > q.hi) continue;
           const uint32_t tS = tbase + lane_base + kColS + x * 128;
-          const int t = q.t0 + tpos;
+          const int t = q.a0 + tpos;  // position of this row's query
           if (!fail) fail = !mbar_wait(s_full + x, ns[x] & 1, lim, abort_flag);
           fail = !__all_sync(0xffffffffu, !fail);
           if (fail) continue;  // nothing more this round; the barrier after the rounds decides for everyone
@@ -470,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait(sv[0]);
           tmem_ld_wait(sv[1]);
           const int s0 = j * kBlockN + 64 * h;  // key of this thread's first column
-          const bool full_tile = (j * kBlockN + kBlockN - 1 <= q.t0) &&
-                                 (p.window < 0 || q.t_last - j * kBlockN <= p.window);
+          const bool full_tile = (j * kBlockN + kBlockN - 1 <= q.a0) &&
+                                 (p.window < 0 || q.a_last - j * kBlockN <= p.window);
           if (!full_tile) {
             // visible columns form the interval [lo_c, hi_c]: key <= t, and t - key <= window
             const int hi_c = t - s0;
@@ -558,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free + x);  // the MMA may start the next item's P.V into O_X
         named_bar_sync(kBarAll, 2 * kSoftThreads);  // staging tile written; the row-sum area is free again
-        if (threadIdx.x == 0) {  // rows past T fall outside the tensor and are not written
+        if (threadIdx.x == 0 && it.valid) {  // rows past T fall outside the tensor and are not written
           tma_store_4d(&tmO, sO, 0, it.g * p.G, q.t0, it.b);
           tma_store_4d(&tmO, sO + kHalfBytes, 64, it.g * p.G, q.t0, it.b);
           bulk_commit_group();

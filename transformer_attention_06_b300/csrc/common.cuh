@@ -22,7 +22,8 @@ namespace nc {
 // ---- device status word (read and cleared by nc_attn_get_device_status) ---------------------------------
 enum : unsigned {
   NC_DEV_TIMEOUT = 1u,        // a bounded wait ran out
-  NC_DEV_BAD_CACHE_LEN = 2u,  // decode: cache_lens[b] outside [0, Tcap] (or [0, Tcap-1] with a new key)
+  NC_DEV_BAD_CACHE_LEN = 2u,  // cache_lens[b] outside [0, Tcap] (decode; [0, Tcap-1] with a new key;
+                              // chunked prefill: [0, Tcap - Tq])
   NC_DEV_SMEM_BASE = 4u,      // the dynamic shared memory base was less aligned than the kernel's slack allows
 };
 __device__ unsigned int g_status;

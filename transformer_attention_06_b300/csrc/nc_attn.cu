@@ -134,6 +134,7 @@ struct HeldBuffer {
 std::mutex g_ws_mu;
 HeldBuffer g_fwd_ws[16];
 HeldBuffer g_dec_ws[16];
+HeldBuffer g_chunk_ws[16];
 
 // Returns a buffer of at least `bytes` for the current device, grown in stream order; `zero` clears a new buffer.
 // `tag` / `clear_bytes`: when a reused buffer was last used with another tag, its first `clear_bytes` are cleared
@@ -212,6 +213,41 @@ nc_status check_decode_args(const void* q, const void* kcache, const void* vcach
   return NC_OK;
 }
 
+// Launches the attention kernel after a prologue on the same stream, with programmatic dependent launch: the CTAs
+// may start (and set up barriers and TMEM) while the prologue drains; they wait on the prologue grid
+// (griddepcontrol.wait) before touching anything it writes.
+nc_status launch_attention(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mvt,
+                           const CUtensorMap& mo, const nc::fwd::Params& prm, int n_sm, cudaStream_t stream) {
+  set_smem_attr_once(nc::fwd::attn_fwd_kernel, nc::fwd::kSmemBytes, 0);
+  const int grid = std::min(n_sm, prm.n_items);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(nc::fwd::kThreads);
+  cfg.dynamicSmemBytes = nc::fwd::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, nc::fwd::attn_fwd_kernel, mq, mk, mv, mvt, mo, prm) != cudaSuccess)
+    return launch_status();
+  return launch_status();
+}
+
+// Work split of the attention kernel over T query rows: P = 128 / G positions per Q tile; two tiles per item
+// (they share every K/V tile), or one tile per item when pairs would not give every SM of the GPU an item.
+// n_pairs is the number of items per (b, kv head).
+bool fwd_split(int B, int T, int Hq, int Hkv, int n_sm, int& G, int& P, int& n_pairs, int& tiles_per_item) {
+  G = Hq / Hkv;
+  if (G > 128) return false;
+  P = 128 / G;
+  const int n_qtiles = (T + P - 1) / P;
+  tiles_per_item = static_cast<long long>(B) * Hkv * ((n_qtiles + 1) / 2) < n_sm ? 1 : 2;
+  n_pairs = tiles_per_item == 2 ? (n_qtiles + 1) / 2 : n_qtiles;
+  return static_cast<long long>(B) * Hkv * n_pairs <= 0x7fffffffLL;
+}
+
 }  // namespace
 
 // =================================================================================================================
@@ -248,12 +284,8 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
   nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
   if (st != NC_OK) return st;
-  const int G = Hq / Hkv;
-  if (G > 128) return NC_ERR_UNSUPPORTED;
-  const int P = 128 / G;
-  const int n_qtiles = (T + P - 1) / P;
-  const int n_pairs = (n_qtiles + 1) / 2;
-  if (static_cast<long long>(B) * Hkv * n_pairs > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
+  int G = 0, P = 0, n_pairs = 0, tpi = 0;
+  if (!fwd_split(B, T, Hq, Hkv, 0, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
   const size_t need = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return NC_ERR_WORKSPACE;
 
@@ -263,6 +295,7 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   unsigned* item_ctr = reinterpret_cast<unsigned*>(ws + 2ull * static_cast<size_t>(B) * T * (Hq + Hkv) * D);
   const int n_sm = sm_count();
   if (n_sm < 1) return NC_ERR_CUDA;
+  if (!fwd_split(B, T, Hq, Hkv, n_sm, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
 
   CUtensorMap mq, mk, mv, mo;
   if (!make_map_4d(&mq, qn, 128, Hq, T, B, 64, G, P, 1) || !make_map_4d(&mk, kn, 128, Hkv, T, B, 64, 1, 128, 1) ||
@@ -285,25 +318,13 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   prm.P = P;
   prm.n_pairs = n_pairs;
   prm.n_items = B * Hkv * n_pairs;
+  prm.tiles_per_item = tpi;
   prm.item_ctr = item_ctr;
+  prm.pos0 = nullptr;
+  prm.Tk = T;
   prm.window = window;
   prm.wait_limit_ns = kWaitLimitNs;
-  set_smem_attr_once(nc::fwd::attn_fwd_kernel, nc::fwd::kSmemBytes, 0);
-  const int grid = std::min(n_sm, prm.n_items);
-  // Programmatic dependent launch: the CTAs may start (and set up barriers and TMEM) while the prologue drains;
-  // they wait on the prologue grid (griddepcontrol.wait) before touching anything it writes.
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(nc::fwd::kThreads);
-  cfg.dynamicSmemBytes = nc::fwd::kSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, nc::fwd::attn_fwd_kernel, mq, mk, mv, mo, prm) != cudaSuccess) return launch_status();
-  st = launch_status();
+  st = launch_attention(mq, mk, mv, mv, mo, prm, n_sm, stream);
   if (st == NC_OK && k2_end != nullptr && cudaEventRecord(k2_end, stream) != cudaSuccess) return NC_ERR_CUDA;
   return st;
 }
@@ -317,6 +338,91 @@ nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* out, in
   void* ws = held_workspace(g_fwd_ws, need, false, -1, 0, stream);
   if (ws == nullptr) return NC_ERR_CUDA;
   return nc_attn_fwd_ws(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, ws, need, stream);
+}
+
+size_t nc_attn_prefill_chunk_workspace_bytes(int B, int Tq, int Hq, int Hkv, int D) {
+  if (check_fwd_shapes(B, Tq, Hq, Hkv, D) != NC_OK) return 0;
+  // qn [B, Tq, Hq, D], the V tail copies [B, 128, Hkv, D] (bf16), then the work-item counter
+  return 2ull * static_cast<size_t>(B) * Tq * Hq * D + 2ull * static_cast<size_t>(B) * 128 * Hkv * D + 256;
+}
+
+nc_status nc_attn_prefill_chunk_ws(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                                   const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D,
+                                   int Tcap, int window, float rope_base, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  if (q == nullptr || k_new == nullptr || v_new == nullptr || kcache == nullptr || vcache == nullptr ||
+      cache_lens == nullptr || out == nullptr)
+    return NC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(kcache) || !aligned16(vcache) ||
+      !aligned16(out))
+    return NC_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID_ARG;
+  if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
+  nc_status st = check_fwd_shapes(B, Tq, Hq, Hkv, D);
+  if (st != NC_OK) return st;
+  if (Tcap < Tq) return NC_ERR_INVALID_ARG;
+  st = check_fwd_shapes(B, Tcap, Hkv, Hkv, D);  // cache positions exact in fp32, sizes in range
+  if (st != NC_OK) return st;
+  int G = 0, P = 0, n_pairs = 0, tpi = 0;
+  if (!fwd_split(B, Tq, Hq, Hkv, 0, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
+  const size_t need = nc_attn_prefill_chunk_workspace_bytes(B, Tq, Hq, Hkv, D);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return NC_ERR_WORKSPACE;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qn = ws;
+  void* vtail = ws + 2ull * static_cast<size_t>(B) * Tq * Hq * D;
+  unsigned* item_ctr = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(vtail) + 2ull * static_cast<size_t>(B) * 128 * Hkv * D);
+  const int n_sm = sm_count();
+  if (n_sm < 1) return NC_ERR_CUDA;
+  if (!fwd_split(B, Tq, Hq, Hkv, n_sm, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
+
+  CUtensorMap mq, mk, mv, mvt, mo;
+  if (!make_map_4d(&mq, qn, 128, Hq, Tq, B, 64, G, P, 1) ||
+      !make_map_4d(&mk, kcache, 128, Hkv, Tcap, B, 64, 1, 128, 1) ||
+      !make_map_4d(&mv, vcache, 128, Hkv, Tcap, B, 64, 1, 128, 1) ||
+      !make_map_4d(&mvt, vtail, 128, Hkv, 128, B, 64, 1, 128, 1) ||
+      !make_map_4d(&mo, out, 128, Hq, Tq, B, 64, G, P, 1))
+    return NC_ERR_CUDA;
+
+  const int tok_blocks = (B * Tq + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
+  const int tail_blocks = (B * 128 + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
+  nc::chunk_prologue_kernel<<<tok_blocks + tail_blocks, nc::kPrologueThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
+      static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(qn), static_cast<__nv_bfloat16*>(kcache),
+      static_cast<__nv_bfloat16*>(vcache), static_cast<__nv_bfloat16*>(vtail), static_cast<__nv_bfloat16*>(out),
+      cache_lens, B, Tq, Hq, Hkv, Tcap, tok_blocks, rope_table(rope_base), scale_log2_for_d128(), item_ctr);
+  st = launch_status();
+  if (st != NC_OK) return st;
+
+  nc::fwd::Params prm;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.B = B;
+  prm.T = Tq;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.G = G;
+  prm.P = P;
+  prm.n_pairs = n_pairs;
+  prm.n_items = B * Hkv * n_pairs;
+  prm.tiles_per_item = tpi;
+  prm.item_ctr = item_ctr;
+  prm.pos0 = cache_lens;
+  prm.Tk = Tcap;
+  prm.window = window;
+  prm.wait_limit_ns = kWaitLimitNs;
+  return launch_attention(mq, mk, mv, mvt, mo, prm, n_sm, stream);
+}
+
+nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                                const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D, int Tcap,
+                                int window, float rope_base, cudaStream_t stream) {
+  const nc_status st = check_fwd_shapes(B, Tq, Hq, Hkv, D);
+  if (st != NC_OK) return st;
+  const size_t need = nc_attn_prefill_chunk_workspace_bytes(B, Tq, Hq, Hkv, D);
+  void* ws = held_workspace(g_chunk_ws, need, false, -1, 0, stream);
+  if (ws == nullptr) return NC_ERR_CUDA;
+  return nc_attn_prefill_chunk_ws(q, k_new, v_new, kcache, vcache, cache_lens, out, B, Tq, Hq, Hkv, D, Tcap, window,
+                                  rope_base, ws, need, stream);
 }
 
 size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, int window) {

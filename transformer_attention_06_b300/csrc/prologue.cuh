@@ -102,4 +102,72 @@ __global__ void __launch_bounds__(kPrologueThreads)
                   s, gmask, 1.0f);
 }
 
+// Chunked prefill against a KV cache ("nanochat Admin & Developer Guide", section 6, SDPA case 3 "chunked /
+// sliding-window inference"; section 7, the in-place KV-cache append).  For sequence b with p0 = cache_lens[b]:
+//   * the chunk's queries q[b, t] and keys k_new[b, t] are roped at position p0 + t and normed; qn goes to the
+//     workspace (times q_scale), the keys go straight into kcache[b, p0 + t] and the values v_new[b, t] into
+//     vcache[b, p0 + t];
+//   * the V tile that holds the chunk's last key (rows [128 hb, 128 hb + 128), hb = (p0 + Tq - 1) / 128) is copied
+//     into vtail[b] with the rows past the chunk set to zero, so that the attention kernel never multiplies a zero
+//     probability by whatever the cache holds beyond its valid rows;
+//   * a sequence whose p0 is outside [0, Tcap - Tq] gets a zero output, its cache is left alone and the device
+//     status records NC_DEV_BAD_CACHE_LEN.
+// Blocks [0, n_tok_blocks) take one token per 8-lane group, the rest one row of a V tail copy per group.
+__global__ void __launch_bounds__(kPrologueThreads)
+    chunk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
+                          const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ qn,
+                          __nv_bfloat16* kcache, __nv_bfloat16* vcache, __nv_bfloat16* __restrict__ vtail,
+                          __nv_bfloat16* __restrict__ out, const int* __restrict__ cache_lens, int B, int Tq, int Hq,
+                          int Hkv, int Tcap, int n_tok_blocks, const __grid_constant__ RopeTable tab, float q_scale,
+                          unsigned* zero_word) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0u;
+  const int grp = threadIdx.x >> 3;
+  const int kq = threadIdx.x & 7;
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  if (static_cast<int>(blockIdx.x) < n_tok_blocks) {
+    const int tok = blockIdx.x * kPrologueTokensPerBlock + grp;
+    if (tok >= B * Tq) return;  // whole 8-lane groups leave together
+    const int b = tok / Tq, t = tok - b * Tq;
+    const int p0 = __ldg(cache_lens + b);
+    if (p0 < 0 || p0 > Tcap - Tq) {
+      uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(tok) * Hq * 128);
+      for (int i = kq; i < Hq * 16; i += 8) o[i] = zero4;
+      if (t == 0 && kq == 0) raise_status(NC_DEV_BAD_CACHE_LEN);
+      return;
+    }
+    const unsigned gmask = 0xFFu << ((threadIdx.x & 31) & ~7);
+    const int pos = p0 + t;
+    float c[8], s[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rope_cos_sin(static_cast<float>(pos), tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
+    const size_t row = static_cast<size_t>(b) * Tcap + pos;  // cache row of this token
+    rope_norm_heads(q + static_cast<size_t>(tok) * Hq * 128, qn + static_cast<size_t>(tok) * Hq * 128, Hq, kq, c, s,
+                    gmask, q_scale);
+    rope_norm_heads(k_new + static_cast<size_t>(tok) * Hkv * 128, kcache + row * Hkv * 128, Hkv, kq, c, s, gmask,
+                    1.0f);
+    const uint4* vs = reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(tok) * Hkv * 128);
+    uint4* vd = reinterpret_cast<uint4*>(vcache + row * Hkv * 128);
+    for (int i = kq; i < Hkv * 16; i += 8) vd[i] = __ldg(vs + i);
+    return;
+  }
+  // V tail copy: row i of sequence b
+  const int id = (blockIdx.x - n_tok_blocks) * kPrologueTokensPerBlock + grp;
+  if (id >= B * 128) return;
+  const int b = id >> 7, i = id & 127;
+  const int p0 = __ldg(cache_lens + b);
+  if (p0 < 0 || p0 > Tcap - Tq) return;
+  const int key = ((p0 + Tq - 1) / 128) * 128 + i;
+  uint4* d = reinterpret_cast<uint4*>(vtail + (static_cast<size_t>(b) * 128 + i) * Hkv * 128);
+  if (key < p0) {  // an earlier cache row (not written by this kernel)
+    const uint4* src = reinterpret_cast<const uint4*>(vcache + (static_cast<size_t>(b) * Tcap + key) * Hkv * 128);
+    for (int e = kq; e < Hkv * 16; e += 8) d[e] = src[e];
+  } else if (key < p0 + Tq) {  // a row of the chunk
+    const uint4* src = reinterpret_cast<const uint4*>(v_new + (static_cast<size_t>(b) * Tq + (key - p0)) * Hkv * 128);
+    for (int e = kq; e < Hkv * 16; e += 8) d[e] = __ldg(src + e);
+  } else {
+    for (int e = kq; e < Hkv * 16; e += 8) d[e] = zero4;
+  }
+}
+
 }  // namespace nc

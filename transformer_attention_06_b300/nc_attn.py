@@ -44,6 +44,9 @@ def _load():
         "nc_attn_fwd_ws_events": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp, vp, vp]),
         "nc_attn_qk_prologue": (i, [vp, vp, vp, vp, i, i, i, i, i, f, vp]),
         "nc_attn_decode_workspace_bytes": (sz, [i, i, i, i, i, i]),
+        "nc_attn_prefill_chunk_workspace_bytes": (sz, [i, i, i, i, i]),
+        "nc_attn_prefill_chunk_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, vp]),
+        "nc_attn_prefill_chunk": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]),
         "nc_attn_decode_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp]),
         "nc_attn_decode": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
         "nc_attn_decode_noalloc": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
@@ -123,6 +126,10 @@ def nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D=128):
     return int(lib.nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D))
 
 
+def nc_attn_prefill_chunk_workspace_bytes(B, Tq, Hq, Hkv, D=128):
+    return int(lib.nc_attn_prefill_chunk_workspace_bytes(B, Tq, Hq, Hkv, D))
+
+
 def nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window):
     return int(lib.nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window))
 
@@ -172,6 +179,45 @@ def nc_attn_qk_prologue(q, k, qn=None, kn=None, rope_base=ROPE_BASE, stream=None
                                  _stream(stream))
     _check(st, "nc_attn_qk_prologue")
     return qn, kn
+
+
+def nc_attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, out=None, window=-1, rope_base=ROPE_BASE,
+                          workspace=None, stream=None):
+    """Chunked prefill against a KV cache.  q [B,Tq,Hq,D], k_new / v_new [B,Tq,Hkv,D] (raw), caches
+    [B,Tcap,Hkv,D], cache_lens int32 [B] (device) -> out [B,Tq,Hq,D].
+
+    The chunk's keys (roped at cache_lens[b] + t and normed) and values are written into the caches at rows
+    cache_lens[b] .. cache_lens[b] + Tq - 1; query t attends to the cache rows up to its own position.  cache_lens is
+    not modified.
+    """
+    _need(q, "q", 4)
+    _need(k_new, "k_new", 4)
+    _need(v_new, "v_new", 4)
+    _need(kcache, "kcache", 4)
+    _need(vcache, "vcache", 4)
+    _need(cache_lens, "cache_lens", 1, dtype=torch.int32)
+    B, Tq, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    Tcap = kcache.shape[1]
+    if tuple(k_new.shape) != (B, Tq, Hkv, D) or tuple(v_new.shape) != (B, Tq, Hkv, D):
+        raise ValueError("k_new / v_new must be [B, Tq, Hkv, D]")
+    if tuple(kcache.shape) != (B, Tcap, Hkv, D) or tuple(vcache.shape) != (B, Tcap, Hkv, D):
+        raise ValueError("cache shapes do not match q")
+    if cache_lens.shape[0] != B:
+        raise ValueError("cache_lens must have B entries")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", 4)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have the shape of q")
+    nbytes = nc_attn_prefill_chunk_workspace_bytes(B, Tq, Hq, Hkv, D)
+    if workspace is None:
+        workspace = _workspace("chunk", nbytes, q.device, zero=False)
+    st = lib.nc_attn_prefill_chunk_ws(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(cache_lens),
+                                      _ptr(out), B, Tq, Hq, Hkv, D, Tcap, int(window), float(rope_base),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nc_attn_prefill_chunk")
+    return out
 
 
 def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=None, window=-1,
