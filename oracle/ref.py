@@ -35,6 +35,9 @@ import numpy as np
 
 ROPE_BASE = 100000.0
 RMS_EPS = 1e-6
+# QK_GAIN_NOTE: Guide section 3 (QK-norm bullet): after the norm, queries and keys are scaled by 1.2 "split between
+# Q and K", which multiplies every logit by 1.2.  ``qk_gain`` is that factor on the logits (1.0: the plain 1/sqrt(D)
+# scale of the workloads; 1.2: the sharpened QK-norm).
 
 
 def inv_freq(D, base=ROPE_BASE):
@@ -90,7 +93,7 @@ def _softmax_rows(s):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128):
+def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128, qk_gain=1.0):
     """Prefill / training forward of the attention block.
 
     q: [B, T, Hq, D], k and v: [B, T, Hkv, D] (any real dtype; computed in fp64).  Positions are 0..T-1.
@@ -108,7 +111,7 @@ def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128):
     pos = np.broadcast_to(np.arange(T), (B, T))
     qn = qk_prologue(q, pos, rope_base, eps)
     kn = qk_prologue(k, pos, rope_base, eps)
-    scale = 1.0 / np.sqrt(D)
+    scale = qk_gain / np.sqrt(D)   # see QK_GAIN_NOTE
     out = np.zeros((B, T, Hq, D), dtype=np.float64)
     for b in range(B):
         for h in range(Hq):
@@ -124,7 +127,7 @@ def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128):
     return out
 
 
-def attn_fwd_rows(q, k, v, window, rows, rope_base=ROPE_BASE, eps=RMS_EPS):
+def attn_fwd_rows(q, k, v, window, rows, rope_base=ROPE_BASE, eps=RMS_EPS, qk_gain=1.0):
     """Selected output rows of ``attn_fwd``, one by one (for full-size inputs).
 
     rows: iterable of (b, i, h).  Returns an fp64 array [len(rows), D].  Each row is computed from scratch:
@@ -133,7 +136,7 @@ def attn_fwd_rows(q, k, v, window, rows, rope_base=ROPE_BASE, eps=RMS_EPS):
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
     G = Hq // Hkv
-    scale = 1.0 / np.sqrt(D)
+    scale = qk_gain / np.sqrt(D)   # see QK_GAIN_NOTE
     res = []
     for (b, i, h) in rows:
         g = h // G
@@ -149,7 +152,7 @@ def attn_fwd_rows(q, k, v, window, rows, rope_base=ROPE_BASE, eps=RMS_EPS):
 
 
 def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
-                rope_base=ROPE_BASE, eps=RMS_EPS):
+                rope_base=ROPE_BASE, eps=RMS_EPS, qk_gain=1.0):
     """KV-cache single-token decode.
 
     q: [B, Hq, D] raw query of the new token; kcache, vcache: [B, Tcap, Hkv, D] (rows already roped+normed);
@@ -164,7 +167,7 @@ def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
     B, Hq, D = q.shape
     Hkv = kcache.shape[2]
     G = Hq // Hkv
-    scale = 1.0 / np.sqrt(D)
+    scale = qk_gain / np.sqrt(D)   # see QK_GAIN_NOTE
     out = np.zeros((B, Hq, D), dtype=np.float64)
     kn_new = None
     if k_new is not None:
@@ -190,7 +193,8 @@ def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
     return out, kn_new
 
 
-def attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, window, rope_base=ROPE_BASE, eps=RMS_EPS):
+def attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, window, rope_base=ROPE_BASE, eps=RMS_EPS,
+                       qk_gain=1.0):
     """Chunked prefill against a KV cache -- Guide section 6 (the SDPA fallback's chunked / sliding-window
     inference case: the chunk's queries attend to the cache plus the chunk) and section 7 "KV cache" (in-place
     append at cache_seqlens).
@@ -209,7 +213,7 @@ def attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, window, rope
     Hkv = k_new.shape[2]
     Tcap = kcache.shape[1]
     G = Hq // Hkv
-    scale = 1.0 / np.sqrt(D)
+    scale = qk_gain / np.sqrt(D)   # see QK_GAIN_NOTE
     out = np.zeros((B, Tq, Hq, D), dtype=np.float64)
     kn_new = np.zeros((B, Tq, Hkv, D), dtype=np.float64)
     for b in range(B):

@@ -144,6 +144,36 @@ def test_two_key_attention_closed_form():
     np.testing.assert_allclose(ref.attn_fwd_rows(q, k, v, -1, [(0, 1, 0)])[0], exp1, rtol=1e-13)
 
 
+@pytest.mark.parametrize("gain", [1.2, 0.5, 3.0])
+def test_qk_gain_closed_form(gain):
+    """The QK-norm gain (1.2 in the Guide) multiplies both logits of the two-key case above: p_1 =
+    1 / (1 + exp(gain (s_0 - s_1))), through the prefill, one-row, decode and chunk paths."""
+    eps = 1e-6
+    q = np.zeros((1, 2, 1, 2))
+    k = np.zeros((1, 2, 1, 2))
+    q[0, 1, 0] = [1, 0]
+    q[0, 0, 0] = [0.3, -0.7]
+    k[0, 0, 0] = [1, 0]
+    k[0, 1, 0] = [1, 0]
+    v = np.array([[[[1.5, -2.0]], [[0.25, 4.0]]]])
+    r2 = 0.5 + eps
+    s0 = math.cos(1.0) / r2 / math.sqrt(2.0)
+    s1 = 1.0 / r2 / math.sqrt(2.0)
+    p1 = 1.0 / (1.0 + math.exp(gain * (s0 - s1)))
+    exp1 = (1 - p1) * v[0, 0, 0] + p1 * v[0, 1, 0]
+    np.testing.assert_allclose(ref.attn_fwd(q, k, v, -1, qk_gain=gain)[0, 1, 0], exp1, rtol=1e-13)
+    np.testing.assert_allclose(ref.attn_fwd_rows(q, k, v, -1, [(0, 1, 0)], qk_gain=gain)[0], exp1, rtol=1e-13)
+    # decode of position 1 against a cache holding key 0 (roped at 0 = itself, normed) plus key 1 as the new key
+    kc = np.zeros((1, 2, 1, 2))
+    kc[0, 0, 0] = np.array([1.0, 0.0]) / math.sqrt(r2)
+    vc = np.zeros((1, 2, 1, 2))
+    vc[0, 0] = v[0, 0]
+    dec, _ = ref.attn_decode(q[:, 1], kc, vc, np.array([1]), -1, k_new=k[:, 1], v_new=v[:, 1], qk_gain=gain)
+    np.testing.assert_allclose(dec[0, 0], exp1, rtol=1e-12)
+    out, _ = ref.attn_prefill_chunk(q[:, 1:], k[:, 1:], v[:, 1:], kc, vc, [1], -1, qk_gain=gain)
+    np.testing.assert_allclose(out[0, 0, 0], exp1, rtol=1e-12)
+
+
 # ----------------------------------------------------------------------------------------------------------
 # Attention: brute force on tiny inputs
 # ----------------------------------------------------------------------------------------------------------
