@@ -119,6 +119,28 @@ nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_
                                 const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D, int Tcap,
                                 int window, float rope_base, cudaStream_t stream);
 
+/* ---- QK-norm gain ----------------------------------------------------------------------------------------------
+ * ("nanochat Admin & Developer Guide", section 3, QK-norm bullet: after the norm, queries and keys are scaled by 1.2,
+ * split between Q and K, for sharper attention.)  The _ex entry points take that factor as `qk_gain`: every logit is
+ * qk_gain * qn.kn / sqrt(D).  qk_gain = 1 is the plain forms above; 1.2 is nanochat's.  Accepted range (0, 4]: the
+ * prefill kernel's softmax takes exponentials without a running maximum, which the bound |logit| <= 16.5 qk_gain
+ * (in base 2, for unit-RMS q and k) keeps within fp32 and bf16 up to a gain of 4; NC_ERR_INVALID_ARG otherwise.
+ * All other arguments, layouts, workspaces and errors as for the corresponding _ws entry point.
+ */
+nc_status nc_attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                         int D, int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+nc_status nc_attn_prefill_chunk_ex(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                                   const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D,
+                                   int Tcap, int window, float rope_base, float qk_gain, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
+
+nc_status nc_attn_decode_ex(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                            const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
+                            int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
 /* ---- KV-cache single-token decode ------------------------------------------------------------------------------
  * One new query token per sequence b, at position p_b = cache_lens[b].
  *   q:[B,Hq,D]            raw query of the new token (roped at position p_b, then normed, inside the call)

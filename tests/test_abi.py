@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nc_attn_fwd", "nc_attn_fwd_ws", "nc_attn_decode", "nc_attn_decode_ws", "nc_attn_status_string",
-              "nc_attn_get_device_status", "nc_attn_qk_prologue", "nc_attn_prefill_chunk", "nc_attn_prefill_chunk_ws"):
+              "nc_attn_get_device_status", "nc_attn_qk_prologue", "nc_attn_prefill_chunk", "nc_attn_prefill_chunk_ws",
+              "nc_attn_fwd_ex", "nc_attn_prefill_chunk_ex", "nc_attn_decode_ex"):
         assert n in names
 
 
@@ -125,6 +126,20 @@ def test_prefill_chunk_rejects_bad_arguments(nc):
     need = nc.nc_attn_prefill_chunk_workspace_bytes(2, 100, 6, 2)
     assert chunk(nc, ws=P, wsb=need - 1) == WS
     assert chunk(nc, ws=PM, wsb=need) == WS
+
+
+def test_qk_gain_range_is_checked(nc):
+    # (0, 4]: outside it the prefill softmax's bound on the logits would not hold; checked before anything else
+    E = nc.NC_ERR_INVALID_ARG
+    for g in (0.0, -1.0, 4.01, float("nan"), float("inf")):
+        assert nc.lib.nc_attn_fwd_ex(P, P, P, P, 1, 256, 4, 2, 128, -1, 1e5, g, None, 0, None) == E
+        assert nc.lib.nc_attn_prefill_chunk_ex(P, P, P, P, P, P, P, 2, 100, 6, 2, 128, 300, -1, 1e5, g, None, 0,
+                                               None) == E
+        assert nc.lib.nc_attn_decode_ex(P, P, P, P, P, None, None, 4, 12, 4, 128, 64, -1, 1e5, g, None, 0, None) == E
+    # a valid gain reaches the next check (the missing workspace)
+    assert nc.lib.nc_attn_fwd_ex(P, P, P, P, 1, 256, 4, 2, 128, -1, 1e5, 4.0, None, 0, None) == nc.NC_ERR_WORKSPACE
+    assert nc.lib.nc_attn_decode_ex(P, P, P, P, P, None, None, 4, 12, 4, 128, 64, -1, 1e5, 1.2, None, 0,
+                                    None) == nc.NC_ERR_WORKSPACE
 
 
 def test_workspace_sizes(nc):

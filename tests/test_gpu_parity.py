@@ -69,6 +69,9 @@ ODD = [  # (B, T, Hq, Hkv, W): T not a multiple of the tile, ragged tails, every
     (2, 160, 4, 4, 128),
     (1, 65, 32, 1, -1),
     (1, 700, 2, 2, 300),
+    (1, 33, 128, 1, -1),     # largest group: one position per tile
+    (1, 70, 64, 1, 20),
+    (2, 77, 10, 2, 30),      # group of 5: 125 of the 128 tile rows in use
 ]
 
 

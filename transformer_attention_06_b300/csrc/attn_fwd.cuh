@@ -62,11 +62,12 @@ constexpr uint32_t kColO = 256;               // O_X at kColO + 128 X
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);  // A = Q, B = K, both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // A = P (TMEM), B = V (MN-major)
 // Softmax without a running maximum.  kn and qn are RMS-normalised by the prologue (RMSNorm without weight,
-// eps > 0), and qn leaves it multiplied by c = log2(e) / sqrt(128), so the S tile holds base-2 logits.  Before
-// rounding, |kn| <= sqrt(128) and |qn| <= c sqrt(128); bf16 rounding adds at most a factor (1 + 2^-9) to each, so
-// |S| <= c 128 (1 + 2^-9)^2 < 16.5.  P = 2^S then lies in [2^-16.5, 2^16.5] -- no overflow or underflow in fp32
-// or bf16, and row sums of at most 2^31 keys stay far below the fp32 range -- so the exponentials need no offset
-// and neither O nor the row sums ever need rescaling; softmax(x) = 2^S / sum 2^S exactly as with a maximum.
+// eps > 0), and qn leaves it multiplied by c = g log2(e) / sqrt(128) (g: the QK-norm gain, 1 or e.g. 1.2, at most
+// 4), so the S tile holds base-2 logits.  Before rounding, |kn| <= sqrt(128) and |qn| <= c sqrt(128); bf16 rounding
+// adds at most a factor (1 + 2^-9) to each, so |S| <= c 128 (1 + 2^-9)^2 < 16.5 g <= 66.  P = 2^S then lies in
+// [2^-66, 2^66] -- no overflow or underflow in fp32 or bf16, and row sums of at most 2^31 keys stay below 2^97 --
+// so the exponentials need no offset and neither O nor the row sums ever need rescaling; softmax(x) =
+// 2^S / sum 2^S exactly as with a maximum.
 
 constexpr int kOffQ = 0;                                 // Q_A, Q_B
 constexpr int kOffK = kOffQ + 2 * kTileBytes;

@@ -70,6 +70,11 @@ RopeTable rope_table(float base) {
 
 float scale_log2_for_d128() { return static_cast<float>(1.4426950408889634 / std::sqrt(128.0)); }
 
+// Largest accepted gain on the logits.  The prefill kernel takes exponentials without a running maximum: with unit-RMS
+// qn, kn its base-2 logits are bounded by 16.5 times the gain, so a gain of at most 4 keeps 2^S within [2^-66, 2^66]
+// and any row sum below 2^97 (fp32 and bf16 hold both).
+constexpr float kMaxQkGain = 4.0f;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool rope_base_ok(float base) { return std::isfinite(base) && base > 0.f; }
@@ -275,11 +280,12 @@ nc_status nc_attn_fwd_ws(const void* q, const void* k, const void* v, void* out,
                                nullptr, nullptr, nullptr, stream);
 }
 
-nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,
-                                int Hkv, int D, int window, float rope_base, void* workspace,
-                                size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin,
-                                cudaEvent_t k2_end, cudaStream_t stream) {
+static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                          int D, int window, float rope_base, float qk_gain, void* workspace,
+                          size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin, cudaEvent_t k2_end,
+                          cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return NC_ERR_INVALID_ARG;
+  if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NC_ERR_INVALID_ARG;
   if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
   nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
@@ -304,7 +310,8 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
 
   if (k1_begin != nullptr && cudaEventRecord(k1_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
   // qn leaves the prologue multiplied by log2(e) / sqrt(D): the attention kernel's scores are then base-2 logits.
-  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), scale_log2_for_d128(), item_ctr, stream);
+  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), scale_log2_for_d128() * qk_gain, item_ctr,
+                       stream);
   if (st != NC_OK) return st;
   if (k2_begin != nullptr && cudaEventRecord(k2_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
 
@@ -329,6 +336,21 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
   return st;
 }
 
+nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,
+                                int Hkv, int D, int window, float rope_base, void* workspace,
+                                size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin,
+                                cudaEvent_t k2_end, cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, 1.0f, workspace, workspace_bytes, k1_begin,
+                  k2_begin, k2_end, stream);
+}
+
+nc_status nc_attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                         int D, int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace, workspace_bytes, nullptr,
+                  nullptr, nullptr, stream);
+}
+
 nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv, int D,
                       int window, float rope_base, cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return NC_ERR_INVALID_ARG;
@@ -346,10 +368,11 @@ size_t nc_attn_prefill_chunk_workspace_bytes(int B, int Tq, int Hq, int Hkv, int
   return 2ull * static_cast<size_t>(B) * Tq * Hq * D + 2ull * static_cast<size_t>(B) * 128 * Hkv * D + 256;
 }
 
-nc_status nc_attn_prefill_chunk_ws(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
-                                   const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D,
-                                   int Tcap, int window, float rope_base, void* workspace, size_t workspace_bytes,
-                                   cudaStream_t stream) {
+static nc_status chunk_impl(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                            const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D, int Tcap,
+                            int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   if (q == nullptr || k_new == nullptr || v_new == nullptr || kcache == nullptr || vcache == nullptr ||
       cache_lens == nullptr || out == nullptr)
     return NC_ERR_INVALID_ARG;
@@ -390,7 +413,8 @@ nc_status nc_attn_prefill_chunk_ws(const void* q, const void* k_new, const void*
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
       static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(qn), static_cast<__nv_bfloat16*>(kcache),
       static_cast<__nv_bfloat16*>(vcache), static_cast<__nv_bfloat16*>(vtail), static_cast<__nv_bfloat16*>(out),
-      cache_lens, B, Tq, Hq, Hkv, Tcap, tok_blocks, rope_table(rope_base), scale_log2_for_d128(), item_ctr);
+      cache_lens, B, Tq, Hq, Hkv, Tcap, tok_blocks, rope_table(rope_base), scale_log2_for_d128() * qk_gain,
+      item_ctr);
   st = launch_status();
   if (st != NC_OK) return st;
 
@@ -413,6 +437,22 @@ nc_status nc_attn_prefill_chunk_ws(const void* q, const void* k_new, const void*
   return launch_attention(mq, mk, mv, mvt, mo, prm, n_sm, stream);
 }
 
+nc_status nc_attn_prefill_chunk_ws(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                                   const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D,
+                                   int Tcap, int window, float rope_base, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  return chunk_impl(q, k_new, v_new, kcache, vcache, cache_lens, out, B, Tq, Hq, Hkv, D, Tcap, window, rope_base,
+                    1.0f, workspace, workspace_bytes, stream);
+}
+
+nc_status nc_attn_prefill_chunk_ex(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
+                                   const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D,
+                                   int Tcap, int window, float rope_base, float qk_gain, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+  return chunk_impl(q, k_new, v_new, kcache, vcache, cache_lens, out, B, Tq, Hq, Hkv, D, Tcap, window, rope_base,
+                    qk_gain, workspace, workspace_bytes, stream);
+}
+
 nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
                                 const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D, int Tcap,
                                 int window, float rope_base, cudaStream_t stream) {
@@ -431,10 +471,11 @@ size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, i
   return decode_layout(B, Hq, Hkv).total;
 }
 
-nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
-                            const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
-                            int window, float rope_base, void* workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+static nc_status decode_impl(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                             const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
+                             int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   const nc_status st =
       check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
   if (st != NC_OK) return st;
@@ -466,7 +507,7 @@ nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int
   prm.G = Hq / Hkv;
   prm.Tcap = Tcap;
   prm.window = window;
-  prm.scale_log2 = scale_log2_for_d128();
+  prm.scale_log2 = scale_log2_for_d128() * qk_gain;
   prm.wait_limit_ns = kWaitLimitNs;
   const RopeTable tab = rope_table(rope_base);
   switch (prm.G) {
@@ -489,6 +530,22 @@ nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int
     default: return NC_ERR_UNSUPPORTED;
   }
   return launch_status();
+}
+
+nc_status nc_attn_decode_ws(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                            const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
+                            int window, float rope_base, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  return decode_impl(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base, 1.0f,
+                     workspace, workspace_bytes, stream);
+}
+
+nc_status nc_attn_decode_ex(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                            const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
+                            int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  return decode_impl(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base,
+                     qk_gain, workspace, workspace_bytes, stream);
 }
 
 nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,

@@ -44,6 +44,9 @@ def _load():
         "nc_attn_fwd_ws_events": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp, vp, vp]),
         "nc_attn_qk_prologue": (i, [vp, vp, vp, vp, i, i, i, i, i, f, vp]),
         "nc_attn_decode_workspace_bytes": (sz, [i, i, i, i, i, i]),
+        "nc_attn_fwd_ex": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
+        "nc_attn_prefill_chunk_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, f, vp, sz, vp]),
+        "nc_attn_decode_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_prefill_chunk_workspace_bytes": (sz, [i, i, i, i, i]),
         "nc_attn_prefill_chunk_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, sz, vp]),
         "nc_attn_prefill_chunk": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]),
@@ -134,11 +137,13 @@ def nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window):
     return int(lib.nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window))
 
 
-def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=None, stream=None, events=None):
+def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=None, stream=None, events=None,
+                qk_gain=1.0):
     """Prefill / training forward.  q [B,T,Hq,D], k and v [B,T,Hkv,D] (bf16, CUDA, contiguous) -> out [B,T,Hq,D].
 
     ``events``: optional (k1_begin, k2_begin, k2_end) torch.cuda.Event objects (any may be None), recorded on the
-    stream around the prologue kernel and the attention kernel.
+    stream around the prologue kernel and the attention kernel.  ``qk_gain``: factor on every logit (the QK-norm
+    gain, 1.2 in nanochat; ``nc_attn_fwd_ex``); not combined with ``events``.
     """
     _need(q, "q", 4)
     _need(k, "k", 4)
@@ -155,10 +160,17 @@ def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=Non
     nbytes = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D)
     if workspace is None:
         workspace = _workspace("fwd", nbytes, q.device, zero=False)
+    wsb = workspace.numel() * workspace.element_size()
+    if qk_gain != 1.0:
+        if events is not None:
+            raise ValueError("events are recorded only with qk_gain = 1")
+        st = lib.nc_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, D, int(window), float(rope_base),
+                                float(qk_gain), _ptr(workspace), wsb, _stream(stream))
+        _check(st, "nc_attn_fwd")
+        return out
     ev = [_event_handle(e, stream) for e in (events or (None, None, None))]
     st = lib.nc_attn_fwd_ws_events(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, D, int(window),
-                                   float(rope_base), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                   ev[0], ev[1], ev[2], _stream(stream))
+                                   float(rope_base), _ptr(workspace), wsb, ev[0], ev[1], ev[2], _stream(stream))
     _check(st, "nc_attn_fwd")
     return out
 
@@ -182,7 +194,7 @@ def nc_attn_qk_prologue(q, k, qn=None, kn=None, rope_base=ROPE_BASE, stream=None
 
 
 def nc_attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, out=None, window=-1, rope_base=ROPE_BASE,
-                          workspace=None, stream=None):
+                          workspace=None, stream=None, qk_gain=1.0):
     """Chunked prefill against a KV cache.  q [B,Tq,Hq,D], k_new / v_new [B,Tq,Hkv,D] (raw), caches
     [B,Tcap,Hkv,D], cache_lens int32 [B] (device) -> out [B,Tq,Hq,D].
 
@@ -213,15 +225,16 @@ def nc_attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, out=None,
     nbytes = nc_attn_prefill_chunk_workspace_bytes(B, Tq, Hq, Hkv, D)
     if workspace is None:
         workspace = _workspace("chunk", nbytes, q.device, zero=False)
-    st = lib.nc_attn_prefill_chunk_ws(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(cache_lens),
+    st = lib.nc_attn_prefill_chunk_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(cache_lens),
                                       _ptr(out), B, Tq, Hq, Hkv, D, Tcap, int(window), float(rope_base),
-                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+                                      float(qk_gain), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream))
     _check(st, "nc_attn_prefill_chunk")
     return out
 
 
 def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=None, window=-1,
-                   rope_base=ROPE_BASE, workspace=None, stream=None):
+                   rope_base=ROPE_BASE, workspace=None, stream=None, qk_gain=1.0):
     """Single-token decode.  q [B,Hq,D]; caches [B,Tcap,Hkv,D]; cache_lens int32 [B] (device) -> out [B,Hq,D].
 
     With k_new / v_new [B,Hkv,D], the new key (roped + normed at cache_lens[b]) and value are written into the caches
@@ -254,9 +267,9 @@ def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=No
         if _ws_decode_tag.get(key, B * Hkv) != B * Hkv:
             workspace.zero_()
         _ws_decode_tag[key] = B * Hkv
-    st = lib.nc_attn_decode_ws(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
-                               _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base), _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream))
+    st = lib.nc_attn_decode_ex(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
+                               _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base), float(qk_gain),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nc_attn_decode")
     return out
 
