@@ -49,7 +49,7 @@ constexpr int kKStages = 2;                   // K ring: a stage is free once bo
 constexpr int kVStages = 2;                   // V ring: a stage is free once both P.V products of its tile are done
 constexpr int kHalfBytes = 128 * 128;         // one 64-column half of a 128-row bf16 tile
 constexpr int kTileBytes = 2 * kHalfBytes;    // 32 KB
-constexpr int kSoftThreads = 128;             // one warpgroup per Q tile
+constexpr int kSoftThreads = 128;             // one softmax warpgroup = the 128 rows (TMEM lanes) of a Q tile
 constexpr int kSoftWarps = 8;                 // softmax warps; each arrives once on p_full / o_free
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;                   // MMA issuer of Q tile A; also allocates TMEM
@@ -103,6 +103,7 @@ struct Params {
   unsigned* item_ctr;                 // work-item counter, zero at launch (written by the prologue kernel)
   // Position of query 0 of sequence b (chunked prefill against a cache: the cache length); null means 0.
   const int* pos0;
+  // n_pairs: work items per (b, kv head) (pairs of Q tiles, or single tiles when tiles_per_item is 1)
   int B, T, Hq, Hkv, G, P, n_pairs, n_items, window;
   int tiles_per_item;                 // 2 (Q tiles A and B share every K/V tile), or 1 when pairs would leave SMs idle
   int Tk;                             // key rows per sequence that the K / V maps address (T, or the cache size)
