@@ -40,7 +40,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from seeded_inputs import CHUNK, DECODE, DEPTH12, chunk_inputs, decode_inputs, fwd_inputs  # noqa: E402
+from seeded_inputs import CHUNK, DECODE, DEPTH12, bwd_inputs, chunk_inputs, decode_inputs, fwd_inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (in-band) & % bf16 peak; decode GB/s & % HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -472,6 +472,35 @@ def run_ours(args, ws, rank, local):
                           f"replayed from a CUDA graph after a 512 MiB L2 flush outside the events")}
         del kc, vc
 
+    # ---- backward pass (CUDA-core kernels) on the depth-12 layer shapes
+    bwd = None
+    if not args.skip_decode:
+        bq, bk, bv, bdo = (t.to(dev) for t in bwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=0))
+        bws = torch.empty(int(nc.lib.nc_attn_bwd_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D)), dtype=torch.uint8,
+                          device=dev)
+        per_w, tot_f, tot_us = {}, 0.0, 0.0
+        for W in sorted(set(w.windows)):
+            nc.nc_attn_bwd(bq, bk, bv, bdo, window=W, workspace=bws)
+            torch.cuda.synchronize()
+            n_b = 3
+            evs = [(mk(), mk()) for _ in range(n_b)]
+            for i in range(n_b):
+                flush.fill_(i)
+                evs[i][0].record(stream)
+                nc.nc_attn_bwd(bq, bk, bv, bdo, window=W, workspace=bws)
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+            us = dist_max(sum(a.elapsed_time(b) for a, b in evs) * 1e3 / n_b, ws)
+            fl = 2.5 * fwd_flops(w.B, w.T, w.Hq, w.D, W)
+            per_w[str(W)] = {"us_per_call": us, "tflops": fl / (us * 1e-6) / 1e12}
+            tot_f += fl
+            tot_us += us
+        val = tot_f / (tot_us * 1e-6) / 1e12
+        bwd = {"value": val, "unit": "TFLOP/s", "frac": val / peaks["bf16_tflops"], "windows": per_w,
+               "config": (f"{w.name} layer shapes, windows {sorted(set(w.windows))}; dq, dk, dv in fp32 from CUDA-core "
+                          f"kernels; FLOPs counted as 2.5x the forward's in-band FLOPs; L2 flushed before each call")}
+        del bq, bk, bv, bdo, bws
+
     st = nc.nc_attn_get_device_status(clear=True)
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -500,6 +529,7 @@ def run_ours(args, ws, rank, local):
                          "launches_timed": n_roof * len(layers)},
             "decode": dec,
             "prefill_chunk": chk,
+            "backward": bwd,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": args.steps * len(layers) * 2,

@@ -141,6 +141,22 @@ nc_status nc_attn_decode_ex(const void* q, void* kcache, void* vcache, const int
                             int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream);
 
+/* ---- Backward pass of the prefill forward -----------------------------------------------------------------------
+ * ("nanochat Admin & Developer Guide", section 3: the model trains through this block.)  Gradients of
+ * sum(dout * out), out = nc_attn_fwd_ex(q, k, v, window, rope_base, qk_gain), with respect to the raw q, k, v:
+ *   q:[B,T,Hq,D] k,v:[B,T,Hkv,D] dout:[B,T,Hq,D]  bf16, 16-byte aligned device memory
+ *   dq:[B,T,Hq,D] dk,dv:[B,T,Hkv,D]               fp32, written (not accumulated)
+ * through the RoPE, the weightless RMSNorm and the banded GQA softmax, in fp32 on the CUDA cores.  The workspace
+ * (16-byte aligned, nc_attn_bwd_workspace_bytes(...) bytes, no initialisation) holds the normed vectors and row
+ * statistics.  Errors as nc_attn_fwd_ws (qk_gain in (0, 4]).  The pages have no such entry point; autograd
+ * computes the same gradients there.
+ */
+size_t nc_attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
+
+nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void* dout, float* dq, float* dk,
+                         float* dv, int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ---- KV-cache single-token decode ------------------------------------------------------------------------------
  * One new query token per sequence b, at position p_b = cache_lens[b].
  *   q:[B,Hq,D]            raw query of the new token (roped at position p_b, then normed, inside the call)

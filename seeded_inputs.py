@@ -8,7 +8,8 @@ workloads.  Recipe (the same bf16 tensors go to both sides):
   k-cache, v-cache, cache lengths, q, [k_new, v_new] (decode);
 * each draw is rounded to bfloat16 (round-to-nearest-even) with ``.to(torch.bfloat16)``;
 * decode cache lengths: ``torch.randint(lo, hi + 1, (B,), generator=g)`` (uniform on [lo, hi]);
-* chunked prefill: k-cache, v-cache, q, k_new, v_new in that order; the cache lengths are given, not drawn.
+* chunked prefill: k-cache, v-cache, q, k_new, v_new in that order; the cache lengths are given, not drawn;
+* backward: q, k, v, then the upstream gradient dout.
 
 Values are N(0, 1), the distribution the nanochat workloads below are quoted with.  Shapes follow nanochat
 configurations (depth 12 gives model dim 768 = 6 heads of 128; GQA and long-context variants).
@@ -115,3 +116,13 @@ def chunk_inputs(B, Tq, Hq, Hkv, D, Tcap, seed=0):
     k_new = _randn((B, Tq, Hkv, D), gen)
     v_new = _randn((B, Tq, Hkv, D), gen)
     return dict(kcache=kcache, vcache=vcache, q=q, k_new=k_new, v_new=v_new)
+
+
+def bwd_inputs(B, T, Hq, Hkv, D, seed=0):
+    """Backward inputs as bf16 CPU tensors: q [B,T,Hq,D], k, v [B,T,Hkv,D] and the upstream gradient dout [B,T,Hq,D]."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    q = _randn((B, T, Hq, D), gen)
+    k = _randn((B, T, Hkv, D), gen)
+    v = _randn((B, T, Hkv, D), gen)
+    dout = _randn((B, T, Hq, D), gen)
+    return q, k, v, dout

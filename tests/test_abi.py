@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nc_attn_fwd", "nc_attn_fwd_ws", "nc_attn_decode", "nc_attn_decode_ws", "nc_attn_status_string",
               "nc_attn_get_device_status", "nc_attn_qk_prologue", "nc_attn_prefill_chunk", "nc_attn_prefill_chunk_ws",
-              "nc_attn_fwd_ex", "nc_attn_prefill_chunk_ex", "nc_attn_decode_ex"):
+              "nc_attn_fwd_ex", "nc_attn_prefill_chunk_ex", "nc_attn_decode_ex", "nc_attn_bwd_ws"):
         assert n in names
 
 
@@ -140,6 +140,25 @@ def test_qk_gain_range_is_checked(nc):
     assert nc.lib.nc_attn_fwd_ex(P, P, P, P, 1, 256, 4, 2, 128, -1, 1e5, 4.0, None, 0, None) == nc.NC_ERR_WORKSPACE
     assert nc.lib.nc_attn_decode_ex(P, P, P, P, P, None, None, 4, 12, 4, 128, 64, -1, 1e5, 1.2, None, 0,
                                     None) == nc.NC_ERR_WORKSPACE
+
+
+def test_bwd_rejects_bad_arguments(nc):
+    E, U, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_UNSUPPORTED, nc.NC_ERR_WORKSPACE
+    f = nc.lib.nc_attn_bwd_ws
+
+    def call(q=P, dq=P, B=1, T=64, Hq=4, Hkv=2, D=128, W=-1, gain=1.0, ws=None, wsb=0):
+        return f(q, P, P, P, dq, P, P, B, T, Hq, Hkv, D, W, 1e5, gain, ws, wsb, None)
+    assert call(q=None) == E
+    assert call(dq=None) == E
+    assert call(dq=PM) == E
+    assert call(Hq=3, Hkv=2) == E
+    assert call(W=-2) == E
+    assert call(gain=0.0) == E
+    assert call(D=64) == U
+    assert call() == WS
+    need = nc.lib.nc_attn_bwd_workspace_bytes(1, 64, 4, 2, 128)
+    assert need >= 4 * 64 * 6 * 128
+    assert call(ws=P, wsb=need - 1) == WS
 
 
 def test_workspace_sizes(nc):

@@ -14,6 +14,7 @@
 #include "prologue.cuh"
 #include "attn_fwd.cuh"
 #include "attn_decode.cuh"
+#include "attn_bwd.cuh"
 
 namespace {
 
@@ -463,6 +464,81 @@ nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_
   if (ws == nullptr) return NC_ERR_CUDA;
   return nc_attn_prefill_chunk_ws(q, k_new, v_new, kcache, vcache, cache_lens, out, B, Tq, Hq, Hkv, D, Tcap, window,
                                   rope_base, ws, need, stream);
+}
+
+// Backward workspace: qn, kn (fp32), then 1/r of q and k rows, log-sum-exp and rowsum(dO * O) per query row, each
+// region 256-byte aligned.
+struct BwdLayout {
+  size_t qn, kn, inv_rq, inv_rk, lse, drow, total;
+};
+
+static BwdLayout bwd_layout(int B, int T, int Hq, int Hkv) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t rq = static_cast<size_t>(B) * T * Hq, rk = static_cast<size_t>(B) * T * Hkv;
+  BwdLayout L;
+  L.qn = 0;
+  L.kn = up(L.qn + rq * 128 * 4);
+  L.inv_rq = up(L.kn + rk * 128 * 4);
+  L.inv_rk = up(L.inv_rq + rq * 4);
+  L.lse = up(L.inv_rk + rk * 4);
+  L.drow = up(L.lse + rq * 4);
+  L.total = up(L.drow + rq * 4);
+  return L;
+}
+
+size_t nc_attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
+  if (check_fwd_shapes(B, T, Hq, Hkv, D) != NC_OK) return 0;
+  return bwd_layout(B, T, Hq, Hkv).total;
+}
+
+nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void* dout, float* dq, float* dk,
+                         float* dv, int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||
+      dv == nullptr)
+    return NC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return NC_ERR_INVALID_ARG;
+  if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
+  if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
+  const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
+  if (st != NC_OK) return st;
+  const long long rows = static_cast<long long>(B) * T * (Hq + Hkv);
+  if (rows / nc::bwd::kWarpsPerBlock + 1 > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
+  const BwdLayout L = bwd_layout(B, T, Hq, Hkv);
+  if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return NC_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  nc::bwd::Params p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.qn = reinterpret_cast<float*>(ws + L.qn);
+  p.kn = reinterpret_cast<float*>(ws + L.kn);
+  p.inv_rq = reinterpret_cast<float*>(ws + L.inv_rq);
+  p.inv_rk = reinterpret_cast<float*>(ws + L.inv_rk);
+  p.lse = reinterpret_cast<float*>(ws + L.lse);
+  p.drow = reinterpret_cast<float*>(ws + L.drow);
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.window = window;
+  p.c = static_cast<float>(static_cast<double>(qk_gain) / std::sqrt(128.0));
+  const RopeTable tab = rope_table(rope_base);
+  constexpr int kThr = nc::bwd::kWarpsPerBlock * 32;
+  auto blocks = [](long long n) { return static_cast<unsigned>((n + nc::bwd::kWarpsPerBlock - 1) / nc::bwd::kWarpsPerBlock); };
+  const long long nq = static_cast<long long>(B) * T * Hq, nk = static_cast<long long>(B) * T * Hkv;
+  nc::bwd::bwd_prep_kernel<<<blocks(nq + nk), kThr, 0, stream>>>(p, tab);
+  nc::bwd::bwd_rowstats_kernel<<<blocks(nq), kThr, 0, stream>>>(p);
+  nc::bwd::bwd_dq_kernel<<<blocks(nq), kThr, 0, stream>>>(p, tab);
+  nc::bwd::bwd_dkv_kernel<<<blocks(nk), kThr, 0, stream>>>(p, tab);
+  return launch_status();
 }
 
 size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, int window) {

@@ -45,6 +45,8 @@ def _load():
         "nc_attn_qk_prologue": (i, [vp, vp, vp, vp, i, i, i, i, i, f, vp]),
         "nc_attn_decode_workspace_bytes": (sz, [i, i, i, i, i, i]),
         "nc_attn_fwd_ex": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
+        "nc_attn_bwd_workspace_bytes": (sz, [i, i, i, i, i]),
+        "nc_attn_bwd_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_prefill_chunk_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_decode_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_prefill_chunk_workspace_bytes": (sz, [i, i, i, i, i]),
@@ -173,6 +175,30 @@ def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=Non
                                    float(rope_base), _ptr(workspace), wsb, ev[0], ev[1], ev[2], _stream(stream))
     _check(st, "nc_attn_fwd")
     return out
+
+
+def nc_attn_bwd(q, k, v, dout, window=-1, rope_base=ROPE_BASE, qk_gain=1.0, workspace=None, stream=None):
+    """Gradients of sum(dout * nc_attn_fwd(q, k, v, window, qk_gain=...)) with respect to q, k, v.
+
+    q, dout [B,T,Hq,D] and k, v [B,T,Hkv,D] (bf16, CUDA, contiguous) -> (dq, dk, dv) fp32 tensors of the same shapes.
+    """
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, name, 4)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, T, Hkv, D) or tuple(v.shape) != (B, T, Hkv, D) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("k / v / dout shapes do not match q")
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    nbytes = int(lib.nc_attn_bwd_workspace_bytes(B, T, Hq, Hkv, D))
+    if workspace is None:
+        workspace = _workspace("bwd", nbytes, q.device, zero=False)
+    st = lib.nc_attn_bwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, T, Hq, Hkv, D,
+                            int(window), float(rope_base), float(qk_gain), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nc_attn_bwd")
+    return dq, dk, dv
 
 
 def nc_attn_qk_prologue(q, k, qn=None, kn=None, rope_base=ROPE_BASE, stream=None):
