@@ -12,9 +12,13 @@
  *   - "nanochat (Fucina port)", section "Architecture": half-split RoPE with an inverse-built table,
  *     no-weight RMSNorm, grouped causal attention.
  *
+ * Entry points: the prefill forward (nc_attn_fwd*), the chunked prefill against a KV cache (nc_attn_prefill_chunk*),
+ * the single-token decode (nc_attn_decode*), the same three with a QK-norm gain on the logits (*_ex), the backward
+ * pass of the prefill (nc_attn_bwd_ws), the RoPE + norm kernel alone (nc_attn_qk_prologue), and status helpers.
+ *
  * Conventions for every entry point
  *   - Tensors are bfloat16 (passed as void*, 16-bit storage), contiguous, row-major, in DEVICE memory owned by
- *     the caller, and 16-byte aligned.  cache_lens is a device int32 array.
+ *     the caller, and 16-byte aligned (the backward's gradients are fp32).  cache_lens is a device int32 array.
  *   - D (head dim) must be 128; otherwise NC_ERR_UNSUPPORTED.
  *   - Every call is asynchronous on `stream` (0 = legacy default stream) and never synchronizes.  Arguments are
  *     checked on the host before anything is launched; an error return means nothing was launched.
@@ -24,7 +28,8 @@
  *   - window: -1 means unbounded (plain causal).  window >= 0 means key position j is visible to query position
  *     i iff 0 <= i - j <= window (window + 1 keys including the query's own position).
  *   - Arithmetic: bf16 operands, fp32 accumulation and softmax; the softmax probabilities are rounded to bf16
- *     before the P.V product; outputs are rounded to bf16 (round to nearest even).
+ *     before the P.V product; outputs are rounded to bf16 (round to nearest even).  The backward pass computes in
+ *     fp32 throughout.
  *   - Device-side problems never trap.  They set a sticky device status word that nc_attn_get_device_status()
  *     returns: a bounded wait that ran out (NC_ERR_DEVICE_TIMEOUT) or a cache length outside the cache
  *     (NC_ERR_DEVICE_BAD_INPUT; that row's output is written as zeros).
