@@ -427,23 +427,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(k_empty + kv % kKStages);
         for (int j = it.lo; ok && j <= it.hi; ++j, ++kv) {
           const int vst = kv % kVStages, kst1 = (kv + 1) % kKStages;
+          const bool more = j < it.hi;
+          // Every wait of the round comes first, so that P.V(j) and the next S go into the tensor core back to back
+          // (a gap between them lets its pipeline drain).  K(j+1) has normally landed a round earlier.
           if (!(ok = wait(v_full + vst, (kv / kVStages) & 1))) break;
-          if (j >= lo_x && j <= hi_x) {  // O_X += P_X V_j
+          if (more && !(ok = wait(k_full + kst1, ((kv + 1) / kKStages) & 1))) break;
+          const bool pv = j >= lo_x && j <= hi_x;
+          if (pv) {
             if (j == lo_x && nit > 0 && !(ok = wait(o_free + x, (nit - 1) & 1))) break;
             if (!(ok = wait(p_full + x, ns & 1))) break;
-            tc_fence_after_sync();
+          }
+          tc_fence_after_sync();
+          if (pv) {  // O_X += P_X V_j
             issue_pv(vst, j > lo_x ? 1u : 0u);
             ++ns;
           }
+          if (more && j + 1 >= lo_x && j + 1 <= hi_x) issue_s(kst1);  // S_X = Q_X K_{j+1}^T
           commit(v_empty + vst);
-          if (j < it.hi) {
-            if (!(ok = wait(k_full + kst1, ((kv + 1) / kKStages) & 1))) break;
-            if (j + 1 >= lo_x && j + 1 <= hi_x) {  // S_X = Q_X K_{j+1}^T
-              tc_fence_after_sync();
-              issue_s(kst1);
-            }
-            commit(k_empty + kst1);
-          }
+          if (more) commit(k_empty + kst1);
         }
         if (!ok) break;
         commit(q_empty);
