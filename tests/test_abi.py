@@ -191,3 +191,29 @@ def test_binding_rejects_host_tensors(nc):
         nc.nc_attn_fwd(q, q, q)
     with pytest.raises(ValueError):
         nc.nc_attn_decode(q[:, 0], q, q, torch.zeros(1, dtype=torch.int32))
+
+
+def test_a_c_program_links_and_calls_the_library(tmp_path):
+    """The boundary is plain C: a C99 translation unit includes the header, links libnc_attn.so and calls host-only
+    entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    from transformer_attention_06_b300 import nc_attn
+    src = tmp_path / "caller.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "nc_attn.h"\n'
+        "int main(void) {\n"
+        "  size_t n = nc_attn_fwd_workspace_bytes(4, 2048, 6, 6, 128);\n"
+        "  nc_status s = nc_attn_fwd_ws(0, 0, 0, 0, 1, 8, 2, 2, 128, -1, 1e5f, 0, 0, 0);\n"
+        '  printf("%zu %d %s\\n", n, (int)s, nc_attn_status_string(s));\n'
+        "  return 0;\n}\n")
+    libdir = os.path.dirname(nc_attn.LIB_PATH)
+    exe = tmp_path / "caller"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-o", str(exe), str(src), "-I", os.path.dirname(HEADER), "-I", cuda_inc,
+                    "-L", libdir, "-lnc_attn", f"-Wl,-rpath,{libdir}"], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == nc_attn.nc_attn_fwd_workspace_bytes(4, 2048, 6, 6)
+    assert int(out[1]) == nc_attn.NC_ERR_INVALID_ARG
