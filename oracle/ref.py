@@ -93,7 +93,7 @@ def _softmax_rows(s):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128, qk_gain=1.0):
+def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128, qk_gain=1.0, ve=None, ve_gate=None):
     """Prefill / training forward of the attention block.
 
     q: [B, T, Hq, D], k and v: [B, T, Hkv, D] (any real dtype; computed in fp64).  Positions are 0..T-1.
@@ -102,7 +102,7 @@ def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128, qk_ga
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
-    v = np.asarray(v, dtype=np.float64)
+    v = value_mix(v, ve, ve_gate)
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
     if Hq % Hkv:
@@ -125,6 +125,17 @@ def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128, qk_ga
                 s = np.where(mask, s, -np.inf)
                 out[b, i0:i1, h] = _softmax_rows(s) @ v[b, j0:j1, g]
     return out
+
+
+def value_mix(v, ve=None, ve_gate=None):
+    """Values with the gated value embedding mixed in -- Guide section 3 / the parity list's "Value embeddings +
+    gates, ResFormer-style, sigmoid gate".  The pages give no formula; the reading taken is the plainest one:
+    v' = v + sigmoid(g) * ve, with one gate logit g per (token, kv head) and ve of v's shape.  Without ve, v."""
+    v = np.asarray(v, dtype=np.float64)
+    if ve is None:
+        return v
+    g = np.asarray(ve_gate, dtype=np.float64)
+    return v + (1.0 / (1.0 + np.exp(-g)))[..., None] * np.asarray(ve, dtype=np.float64)
 
 
 def attn_fwd_rows(q, k, v, window, rows, rope_base=ROPE_BASE, eps=RMS_EPS, qk_gain=1.0):

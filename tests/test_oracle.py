@@ -174,6 +174,20 @@ def test_qk_gain_closed_form(gain):
     np.testing.assert_allclose(out[0, 0, 0], exp1, rtol=1e-12)
 
 
+def test_value_gate_by_linearity():
+    """Attention is linear in v and the gate logit 0 gives the factor 1/2, so out(v, ve, g = 0) = out(v) + out(ve)/2;
+    a gate logit of -60 leaves v as it is (factor ~1e-26), +60 adds ve in full."""
+    q, k, v = (f64(t) for t in fwd_inputs(2, 40, 4, 2, 16, seed=6))
+    ve = np.random.default_rng(1).standard_normal(v.shape)
+    g0 = np.zeros(v.shape[:3])
+    W = 7
+    np.testing.assert_allclose(ref.attn_fwd(q, k, v, W, ve=ve, ve_gate=g0),
+                               ref.attn_fwd(q, k, v, W) + 0.5 * ref.attn_fwd(q, k, ve, W), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ref.attn_fwd(q, k, v, W, ve=ve, ve_gate=g0 - 60), ref.attn_fwd(q, k, v, W), atol=1e-12)
+    np.testing.assert_allclose(ref.attn_fwd(q, k, v, W, ve=ve, ve_gate=g0 + 60), ref.attn_fwd(q, k, v + ve, W),
+                               atol=1e-12)
+
+
 # ----------------------------------------------------------------------------------------------------------
 # Attention: brute force on tiny inputs
 # ----------------------------------------------------------------------------------------------------------
