@@ -146,6 +146,21 @@ nc_status nc_attn_decode_ex(const void* q, void* kcache, void* vcache, const int
                             int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream);
 
+/* ---- Gated value embedding (prefill) ---------------------------------------------------------------------------
+ * (The parity list's "Value embeddings + gates, ResFormer-style, sigmoid gate", nanochat's "Notable architectural
+ * additions".  The pages give no formula; the reading taken: v' = v + sigmoid(g) * ve, one gate logit g per token
+ * and kv head.)  As nc_attn_fwd_ex with the attention run on v' instead of v:
+ *   ve:[B,T,Hkv,D]   value embedding, bf16, 16-byte aligned
+ *   ve_gate:[B,T,Hkv] gate logits, bf16 (2-byte aligned)
+ * v' is formed in fp32 and rounded to bf16 inside the call (in the workspace, which must hold
+ * nc_attn_fwd_ve_workspace_bytes(...) bytes).  Both ve and ve_gate are required (NC_ERR_INVALID_ARG otherwise).
+ */
+size_t nc_attn_fwd_ve_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
+
+nc_status nc_attn_fwd_ve(const void* q, const void* k, const void* v, const void* ve, const void* ve_gate, void* out,
+                         int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ---- Backward pass of the prefill forward -----------------------------------------------------------------------
  * ("nanochat Admin & Developer Guide", section 3: the model trains through this block.)  Gradients of
  * sum(dout * out), out = nc_attn_fwd_ex(q, k, v, window, rope_base, qk_gain), with respect to the raw q, k, v:

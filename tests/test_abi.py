@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nc_attn_fwd", "nc_attn_fwd_ws", "nc_attn_decode", "nc_attn_decode_ws", "nc_attn_status_string",
               "nc_attn_get_device_status", "nc_attn_qk_prologue", "nc_attn_prefill_chunk", "nc_attn_prefill_chunk_ws",
-              "nc_attn_fwd_ex", "nc_attn_prefill_chunk_ex", "nc_attn_decode_ex", "nc_attn_bwd_ws"):
+              "nc_attn_fwd_ex", "nc_attn_prefill_chunk_ex", "nc_attn_decode_ex", "nc_attn_bwd_ws", "nc_attn_fwd_ve"):
         assert n in names
 
 
@@ -159,6 +159,19 @@ def test_bwd_rejects_bad_arguments(nc):
     need = nc.lib.nc_attn_bwd_workspace_bytes(1, 64, 4, 2, 128)
     assert need >= 4 * 64 * 6 * 128
     assert call(ws=P, wsb=need - 1) == WS
+
+
+def test_fwd_ve_rejects_bad_arguments(nc):
+    E, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_WORKSPACE
+    f = nc.lib.nc_attn_fwd_ve
+    assert f(P, P, P, None, P, P, 1, 64, 4, 2, 128, -1, 1e5, 1.0, None, 0, None) == E        # no ve
+    assert f(P, P, P, P, None, P, 1, 64, 4, 2, 128, -1, 1e5, 1.0, None, 0, None) == E        # no gate
+    assert f(P, P, P, PM, P, P, 1, 64, 4, 2, 128, -1, 1e5, 1.0, None, 0, None) == E          # misaligned ve
+    assert f(P, P, P, P, P, P, 1, 64, 4, 2, 128, -1, 1e5, 1.0, None, 0, None) == WS
+    need = nc.lib.nc_attn_fwd_ve_workspace_bytes(1, 64, 4, 2, 128)
+    assert need == nc.nc_attn_fwd_workspace_bytes(1, 64, 4, 2) + 2 * 64 * 2 * 128
+    fwd_need = nc.nc_attn_fwd_workspace_bytes(1, 64, 4, 2)
+    assert f(P, P, P, P, P, P, 1, 64, 4, 2, 128, -1, 1e5, 1.0, P, fwd_need, None) == WS      # room for v' missing
 
 
 def test_workspace_sizes(nc):

@@ -108,12 +108,16 @@ void set_smem_attr_once(F* kernel, int bytes, int slot) {
 nc_status launch_status() { return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA; }
 
 nc_status launch_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
-                          const RopeTable& tab, float q_scale, unsigned* zero_word, cudaStream_t stream) {
+                          const RopeTable& tab, float q_scale, unsigned* zero_word, cudaStream_t stream,
+                          const void* v = nullptr, const void* ve = nullptr, const void* ve_gate = nullptr,
+                          void* vmix = nullptr) {
   const int BT = B * T;
   const int blocks = (BT + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
   nc::qk_prologue_kernel<<<blocks, nc::kPrologueThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(qn),
-      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, q_scale, zero_word);
+      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, q_scale, zero_word,
+      static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(ve),
+      static_cast<const __nv_bfloat16*>(ve_gate), static_cast<__nv_bfloat16*>(vmix));
   return launch_status();
 }
 
@@ -284,7 +288,7 @@ nc_status nc_attn_fwd_ws(const void* q, const void* k, const void* v, void* out,
 static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
                           int D, int window, float rope_base, float qk_gain, void* workspace,
                           size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin, cudaEvent_t k2_end,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const void* ve = nullptr, const void* ve_gate = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return NC_ERR_INVALID_ARG;
   if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NC_ERR_INVALID_ARG;
@@ -293,26 +297,32 @@ static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out
   if (st != NC_OK) return st;
   int G = 0, P = 0, n_pairs = 0, tpi = 0;
   if (!fwd_split(B, T, Hq, Hkv, 0, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
-  const size_t need = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
+  if ((ve == nullptr) != (ve_gate == nullptr)) return NC_ERR_INVALID_ARG;
+  if (ve != nullptr && (!aligned16(ve) || (reinterpret_cast<uintptr_t>(ve_gate) & 1u) != 0)) return NC_ERR_INVALID_ARG;
+  const size_t need = ve != nullptr ? nc_attn_fwd_ve_workspace_bytes(B, T, Hq, Hkv, D)
+                                    : nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return NC_ERR_WORKSPACE;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* qn = ws;
   void* kn = ws + 2ull * static_cast<size_t>(B) * T * Hq * D;
   unsigned* item_ctr = reinterpret_cast<unsigned*>(ws + 2ull * static_cast<size_t>(B) * T * (Hq + Hkv) * D);
+  // with a value embedding, the mixed values follow the counter (the fwd workspace size, a multiple of 256)
+  void* vmix = ve != nullptr ? ws + nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D) : nullptr;
+  const void* vsrc = ve != nullptr ? vmix : v;
   const int n_sm = sm_count();
   if (n_sm < 1) return NC_ERR_CUDA;
   if (!fwd_split(B, T, Hq, Hkv, n_sm, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
 
   CUtensorMap mq, mk, mv, mo;
   if (!make_map_4d(&mq, qn, 128, Hq, T, B, 64, G, P, 1) || !make_map_4d(&mk, kn, 128, Hkv, T, B, 64, 1, 128, 1) ||
-      !make_map_4d(&mv, v, 128, Hkv, T, B, 64, 1, 128, 1) || !make_map_4d(&mo, out, 128, Hq, T, B, 64, G, P, 1))
+      !make_map_4d(&mv, vsrc, 128, Hkv, T, B, 64, 1, 128, 1) || !make_map_4d(&mo, out, 128, Hq, T, B, 64, G, P, 1))
     return NC_ERR_CUDA;
 
   if (k1_begin != nullptr && cudaEventRecord(k1_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
   // qn leaves the prologue multiplied by log2(e) / sqrt(D): the attention kernel's scores are then base-2 logits.
   st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), scale_log2_for_d128() * qk_gain, item_ctr,
-                       stream);
+                       stream, v, ve, ve_gate, vmix);
   if (st != NC_OK) return st;
   if (k2_begin != nullptr && cudaEventRecord(k2_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
 
@@ -343,6 +353,19 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
                                 cudaEvent_t k2_end, cudaStream_t stream) {
   return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, 1.0f, workspace, workspace_bytes, k1_begin,
                   k2_begin, k2_end, stream);
+}
+
+size_t nc_attn_fwd_ve_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
+  const size_t base = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
+  return base == 0 ? 0 : base + 2ull * static_cast<size_t>(B) * T * Hkv * D;
+}
+
+nc_status nc_attn_fwd_ve(const void* q, const void* k, const void* v, const void* ve, const void* ve_gate, void* out,
+                         int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (ve == nullptr || ve_gate == nullptr) return NC_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace, workspace_bytes, nullptr,
+                  nullptr, nullptr, stream, ve, ve_gate);
 }
 
 nc_status nc_attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,

@@ -76,13 +76,39 @@ __device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict_
   }
 }
 
+// Gated value embedding (the parity list's "Value embeddings + gates, ResFormer-style, sigmoid gate"; the pages give
+// no formula, the reading is v' = v + sigmoid(g) ve with one gate logit g per token and kv head): the H value
+// vectors of one token, 16-byte slices kq and kq + 8 of each, mixed in fp32 and rounded to bf16.
+__device__ __forceinline__ void mix_values(const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ ve,
+                                           const __nv_bfloat16* __restrict__ gate, __nv_bfloat16* __restrict__ vmix,
+                                           int H, int kq) {
+  for (int h = 0; h < H; ++h) {
+    const float g = __bfloat162float(gate[h]);
+    const float a = 1.f / (1.f + expf(-g));
+#pragma unroll
+    for (int i2 = 0; i2 < 2; ++i2) {
+      const int i = h * 16 + kq + 8 * i2;
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(v) + i);
+      const uint4 e = __ldg(reinterpret_cast<const uint4*>(ve) + i);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, es[4] = {e.x, e.y, e.z, e.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        o[w] = pack_bf16x2(fmaf(a, bf16_lo(es[w]), bf16_lo(xs[w])), fmaf(a, bf16_hi(es[w]), bf16_hi(xs[w])));
+      reinterpret_cast<uint4*>(vmix)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 constexpr int kPrologueThreads = 256;
 constexpr int kPrologueTokensPerBlock = kPrologueThreads / 8;
 
 __global__ void __launch_bounds__(kPrologueThreads)
     qk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                        __nv_bfloat16* __restrict__ qn, __nv_bfloat16* __restrict__ kn, int BT, int T, int Hq,
-                       int Hkv, const __grid_constant__ RopeTable tab, float q_scale, unsigned* zero_word) {
+                       int Hkv, const __grid_constant__ RopeTable tab, float q_scale, unsigned* zero_word,
+                       const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ ve,
+                       const __nv_bfloat16* __restrict__ ve_gate, __nv_bfloat16* __restrict__ vmix) {
   // The attention kernel that follows in stream order may be scheduled now; it waits for this grid to complete
   // before reading anything written here.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -100,6 +126,9 @@ __global__ void __launch_bounds__(kPrologueThreads)
                   gmask, q_scale);
   rope_norm_heads(k + static_cast<size_t>(tok) * Hkv * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq, c,
                   s, gmask, 1.0f);
+  if (ve != nullptr)
+    mix_values(v + static_cast<size_t>(tok) * Hkv * 128, ve + static_cast<size_t>(tok) * Hkv * 128,
+               ve_gate + static_cast<size_t>(tok) * Hkv, vmix + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq);
 }
 
 // Chunked prefill against a KV cache ("nanochat Admin & Developer Guide", section 6, SDPA case 3 "chunked /

@@ -46,6 +46,8 @@ def _load():
         "nc_attn_decode_workspace_bytes": (sz, [i, i, i, i, i, i]),
         "nc_attn_fwd_ex": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_bwd_workspace_bytes": (sz, [i, i, i, i, i]),
+        "nc_attn_fwd_ve_workspace_bytes": (sz, [i, i, i, i, i]),
+        "nc_attn_fwd_ve": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_bwd_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_prefill_chunk_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_decode_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
@@ -140,12 +142,13 @@ def nc_attn_decode_workspace_bytes(B, Hq, Hkv, D, Tcap, window):
 
 
 def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=None, stream=None, events=None,
-                qk_gain=1.0):
+                qk_gain=1.0, ve=None, ve_gate=None):
     """Prefill / training forward.  q [B,T,Hq,D], k and v [B,T,Hkv,D] (bf16, CUDA, contiguous) -> out [B,T,Hq,D].
 
     ``events``: optional (k1_begin, k2_begin, k2_end) torch.cuda.Event objects (any may be None), recorded on the
     stream around the prologue kernel and the attention kernel.  ``qk_gain``: factor on every logit (the QK-norm
-    gain, 1.2 in nanochat; ``nc_attn_fwd_ex``); not combined with ``events``.
+    gain, 1.2 in nanochat; ``nc_attn_fwd_ex``); not combined with ``events``.  ``ve`` [B,T,Hkv,D] and ``ve_gate``
+    [B,T,Hkv] (bf16): gated value embedding, the attention runs on v + sigmoid(ve_gate) * ve (``nc_attn_fwd_ve``).
     """
     _need(q, "q", 4)
     _need(k, "k", 4)
@@ -159,9 +162,24 @@ def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=Non
     _need(out, "out", 4)
     if tuple(out.shape) != tuple(q.shape):
         raise ValueError("out must have the shape of q")
-    nbytes = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D)
+    if ve is not None or ve_gate is not None:
+        nbytes = int(lib.nc_attn_fwd_ve_workspace_bytes(B, T, Hq, Hkv, D))
+    else:
+        nbytes = nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D)
     if workspace is None:
         workspace = _workspace("fwd", nbytes, q.device, zero=False)
+    if ve is not None or ve_gate is not None:
+        if ve is None or ve_gate is None or events is not None:
+            raise ValueError("ve and ve_gate go together, and without events")
+        _need(ve, "ve", 4)
+        _need(ve_gate, "ve_gate", 3)
+        if tuple(ve.shape) != tuple(v.shape) or tuple(ve_gate.shape) != tuple(v.shape[:3]):
+            raise ValueError("ve must have v's shape and ve_gate [B, T, Hkv]")
+        st = lib.nc_attn_fwd_ve(_ptr(q), _ptr(k), _ptr(v), _ptr(ve), _ptr(ve_gate), _ptr(out), B, T, Hq, Hkv, D,
+                                int(window), float(rope_base), float(qk_gain), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+        _check(st, "nc_attn_fwd")
+        return out
     wsb = workspace.numel() * workspace.element_size()
     if qk_gain != 1.0:
         if events is not None:
