@@ -125,8 +125,8 @@ nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_
                                 int window, float rope_base, cudaStream_t stream);
 
 /* ---- QK-norm gain ----------------------------------------------------------------------------------------------
- * ("nanochat Admin & Developer Guide", section 3, QK-norm bullet: after the norm, queries and keys are scaled by 1.2,
- * split between Q and K, for sharper attention.)  The _ex entry points take that factor as `qk_gain`: every logit is
+ * ("nanochat Admin & Developer Guide", section 3, QK-norm bullet: after the norm, q and k carry a combined factor
+ * of 1.2 that sharpens the attention.)  The _ex entry points take that factor as `qk_gain`: every logit is
  * qk_gain * qn.kn / sqrt(D).  qk_gain = 1 is the plain forms above; 1.2 is nanochat's.  Accepted range (0, 4]: the
  * prefill kernel's softmax takes exponentials without a running maximum, which the bound |logit| <= 16.5 qk_gain
  * (in base 2, for unit-RMS q and k) keeps within fp32 and bf16 up to a gain of 4; NC_ERR_INVALID_ARG otherwise.
@@ -147,9 +147,9 @@ nc_status nc_attn_decode_ex(const void* q, void* kcache, void* vcache, const int
                             cudaStream_t stream);
 
 /* ---- Gated value embedding (prefill) ---------------------------------------------------------------------------
- * (The parity list's "Value embeddings + gates, ResFormer-style, sigmoid gate", nanochat's "Notable architectural
- * additions".  The pages give no formula; the reading taken: v' = v + sigmoid(g) * ve, one gate logit g per token
- * and kv head.)  As nc_attn_fwd_ex with the attention run on v' instead of v:
+ * (The catalog pages list value embeddings with a sigmoid gate, in the ResFormer manner, among nanochat's
+ * architectural additions.  The pages give no formula; the reading taken: v' = v + sigmoid(g) * ve, one gate logit g
+ * per token and kv head.)  As nc_attn_fwd_ex with the attention run on v' instead of v:
  *   ve:[B,T,Hkv,D]   value embedding, bf16, 16-byte aligned
  *   ve_gate:[B,T,Hkv] gate logits, bf16 (2-byte aligned)
  * v' is formed in fp32 and rounded to bf16 inside the call (in the workspace, which must hold

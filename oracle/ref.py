@@ -35,8 +35,8 @@ import numpy as np
 
 ROPE_BASE = 100000.0
 RMS_EPS = 1e-6
-# QK_GAIN_NOTE: Guide section 3 (QK-norm bullet): after the norm, queries and keys are scaled by 1.2 "split between
-# Q and K", which multiplies every logit by 1.2.  ``qk_gain`` is that factor on the logits (1.0: the plain 1/sqrt(D)
+# QK_GAIN_NOTE: Guide section 3 (QK-norm bullet): after the norm, q and k carry a combined factor of 1.2, shared
+# between them, so every logit is multiplied by 1.2.  ``qk_gain`` is that factor on the logits (1.0: the plain 1/sqrt(D)
 # scale of the workloads; 1.2: the sharpened QK-norm).
 
 
@@ -128,8 +128,8 @@ def attn_fwd(q, k, v, window, rope_base=ROPE_BASE, eps=RMS_EPS, chunk=128, qk_ga
 
 
 def value_mix(v, ve=None, ve_gate=None):
-    """Values with the gated value embedding mixed in -- Guide section 3 / the parity list's "Value embeddings +
-    gates, ResFormer-style, sigmoid gate".  The pages give no formula; the reading taken is the plainest one:
+    """Values with the gated value embedding mixed in -- the catalog pages ("nanochat (Python)", "nanochat (.NET)")
+    list value embeddings with a sigmoid gate, in the ResFormer manner.  They give no formula; the reading taken is:
     v' = v + sigmoid(g) * ve, with one gate logit g per (token, kv head) and ve of v's shape.  Without ve, v."""
     v = np.asarray(v, dtype=np.float64)
     if ve is None:

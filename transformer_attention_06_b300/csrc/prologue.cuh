@@ -76,7 +76,7 @@ __device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict_
   }
 }
 
-// Gated value embedding (the parity list's "Value embeddings + gates, ResFormer-style, sigmoid gate"; the pages give
+// Gated value embedding (the catalog pages list value embeddings with a sigmoid gate, in the ResFormer manner; they give
 // no formula, the reading is v' = v + sigmoid(g) ve with one gate logit g per token and kv head): the H value
 // vectors of one token, 16-byte slices kq and kq + 8 of each, mixed in fp32 and rounded to bf16.
 __device__ __forceinline__ void mix_values(const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ ve,
