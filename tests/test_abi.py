@@ -64,6 +64,7 @@ def test_fwd_rejects_bad_arguments(nc):
     assert fwd(nc, base=float("nan")) == E
     assert fwd(nc, D=64) == U
     assert fwd(nc, T=1 << 24) == U
+    assert fwd(nc, B=1 << 20, T=1 << 12) == U      # B * T tokens beyond 32-bit indexing
     assert fwd(nc, Hq=256, Hkv=1) == U          # group larger than one 128-row tile
     assert fwd(nc) == WS                        # no workspace
     need = nc.nc_attn_fwd_workspace_bytes(1, 256, 4, 2)
