@@ -241,8 +241,10 @@ nc_status launch_attention(const CUtensorMap& mq, const CUtensorMap& mk, const C
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, nc::fwd::attn_fwd_kernel, mq, mk, mv, mvt, mo, prm) != cudaSuccess)
-    return launch_status();
+  if (cudaLaunchKernelEx(&cfg, nc::fwd::attn_fwd_kernel, mq, mk, mv, mvt, mo, prm) != cudaSuccess) {
+    (void)cudaGetLastError();  // clear it: the failure is reported here
+    return NC_ERR_CUDA;
+  }
   return launch_status();
 }
 
