@@ -1,15 +1,17 @@
 #!/usr/bin/env python3
 """Benchmark of the nanochat attention block on one B300 per rank.  Prints one JSON line (rank 0).
 
-A step is one pass of the prefill forward over the depth-12 SSSL layer pattern: four nc_attn_fwd calls (windows
-1024, 1024, 1024, 2048) on B=4, T=2048, Hq=Hkv=6, D=128, each layer with its own seeded q, k, v (seed = layer
-index), all resident in HBM.  L2 is flushed (512 MiB write) before every timed step, outside the timed events.
-Each call runs the RoPE + QK-norm prologue kernel and the tcgen05 attention kernel.
+A step is one pass of the prefill forward over the long-context workload, the largest of the prefill workloads:
+two nc_attn_fwd calls (windows 1024 and 8192 = full causal) on B=2, T=8192, Hq=12, Hkv=4, D=128, each call with its
+own seeded q, k, v (seed = call index), all resident in HBM.  L2 is flushed (512 MiB write) before every timed step,
+outside the timed events.  Each call runs the RoPE + QK-norm prologue kernel and the tcgen05 attention kernel.
 
 value      in-band TFLOP/s of the whole job: 4 * D * N_vis(T, W) * B * Hq FLOPs per call, summed over the calls of
            all ranks, divided by the device time of the slowest rank (CUDA events, max over ranks).
-roofline   the attention kernel (tensor-core bound): in-band FLOPs of its launches / their CUDA-event durations,
-           against the measured bf16 dense peak.
+roofline   the attention kernel (tensor-core bound) on the same workload: in-band FLOPs of its launches / their
+           CUDA-event durations, against the measured bf16 dense peak.
+prefill    one section per prefill workload (tiny, depth-12 SSSL, GQA, long-context): the step's in-band TFLOP/s, the
+           attention kernel's own TFLOP/s and time per launch for each window, and the prologue's time and GB/s.
 decode     the KV-cache decode step (64 sequences, cache lengths U[1, 4096], Hq=12, Hkv=4, W=2048), GB/s of the
            algorithmic bytes (K/V rows in the window, q, out, lengths, new rows) against the measured HBM peak;
            four cache copies are rotated so that every call reads HBM.
@@ -40,7 +42,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from seeded_inputs import CHUNK, DECODE, DEPTH12, bwd_inputs, chunk_inputs, decode_inputs, fwd_inputs  # noqa: E402
+from seeded_inputs import (CHUNK, DECODE, DEPTH12, GQA, LONG, TINY, bwd_inputs, chunk_inputs,  # noqa: E402
+                           decode_inputs, fwd_inputs)
 
 METRIC = "attention fwd TFLOP/s (in-band) & % bf16 peak; decode GB/s & % HBM peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -240,24 +243,35 @@ def dist_barrier(ws):
 
 
 # ------------------------------------------------------------------------------------------------- CPU (oracle)
-def oracle_fwd_sample(batches=4):
-    """Times the fp64 oracle on `batches` batch rows of one W=1024 layer of the depth-12 workload."""
+def prologue_bytes(B, T, Hq, Hkv, D):
+    """Algorithmic HBM bytes of the RoPE + QK-norm prologue: read q and k, write qn and kn (bf16)."""
+    return 2 * 2 * B * T * (Hq + Hkv) * D
+
+
+def oracle_fwd_sample(wl, W, batches, groups=None):
+    """Times the fp64 oracle on the first `batches` batch rows (and the first `groups` kv-head groups, all when
+    None) of one call of workload `wl` with window W.  Returns (in-band FLOPs, seconds)."""
     from oracle import ref
-    w = DEPTH12
-    q, k, v = (t[:batches].double().numpy() for t in fwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=0))
+    G = wl.Hq // wl.Hkv
+    ng = wl.Hkv if groups is None else groups
+    q, k, v = fwd_inputs(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D, seed=0)
+    q, k, v = (x[:batches].double().numpy() for x in (q[:, :, :ng * G], k[:, :, :ng], v[:, :, :ng]))
     t0 = time.perf_counter()
-    ref.attn_fwd(q, k, v, 1024)
+    ref.attn_fwd(q, k, v, W)
     dt = time.perf_counter() - t0
-    flops = fwd_flops(batches, w.T, w.Hq, w.D, 1024)
-    return flops, dt
+    return fwd_flops(batches, wl.T, ng * G, wl.D, W), dt
 
 
 def cpu_baseline():
-    flops, dt = oracle_fwd_sample(4)
+    """The oracle on the long-context workload: both batch rows of the W=1024 call and batch row 0 of the W=8192
+    call (about 300 in-band GFLOP)."""
+    f1, t1 = oracle_fwd_sample(LONG, 1024, LONG.B)
+    f2, t2 = oracle_fwd_sample(LONG, 8192, 1)
+    flops, dt = f1 + f2, t1 + t2
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"one W=1024 layer of the depth-12 workload (B=4, T=2048, Hq=Hkv=6), numpy fp64, "
-                      f"{flops / 1e9:.2f} in-band GFLOP in {dt:.2f} s on {cpu_model()} "
-                      f"({os.cpu_count()} logical cores)"}
+            "sample": f"long-context workload (B=2, T=8192, Hq=12, Hkv=4): the W=1024 call on both batch rows and "
+                      f"the W=8192 call on batch row 0, numpy fp64, {flops / 1e9:.1f} in-band GFLOP in {dt:.1f} s "
+                      f"on {cpu_model()} ({os.cpu_count()} logical cores)"}
 
 
 def run_reference(args, ws, rank):
@@ -265,93 +279,147 @@ def run_reference(args, ws, rank):
         return
     flops_w, secs = [], []
     for it in range(args.warmup + args.steps):
-        f, dt = oracle_fwd_sample(1)
+        f, dt = oracle_fwd_sample(LONG, 1024, 1, groups=1)
         if it >= args.warmup:
             flops_w.append(f)
             secs.append(dt)
     value = sum(flops_w) / sum(secs) / 1e12
     cores = cpu_threads()
+    sample = ("per step: batch row 0, kv-head group 0 (3 query heads) of the W=1024 call of the long-context "
+              f"workload, numpy fp64, {cpu_model()}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "depth12_sssl_b4_t2048_h6: B=4 T=2048 Hq=Hkv=6 D=128, SSSL windows (1024,1024,1024,2048)",
-                   "reference_step": "batch row 0 of one W=1024 layer per step (bounded sample)"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "per step: batch row 0 of one W=1024 layer of the depth-12 workload, numpy fp64, "
-                                   f"{cpu_model()}"},
+        "config": {"workload": LONG_WORKLOAD, "reference_step": sample + " (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+LONG_WORKLOAD = (f"{LONG.name}: B={LONG.B} T={LONG.T} Hq={LONG.Hq} Hkv={LONG.Hkv} D={LONG.D}, one step = calls with "
+                 f"windows {list(LONG.windows)} (sliding window and full causal), distinct seeded q,k,v per call")
+
+
 # ---------------------------------------------------------------------------------------------------- GPU arm
+def prefill_section(nc, wl, dev, flush, n_steps, n_warmup=3, seeds=None):
+    """Times one prefill workload: a step is one call per window of `wl` (call i on inputs of seed i, or seeds[i]).
+
+    Returns (section dict, per-step event times in ms, layer tensors, workspace).  The step time comes from CUDA-graph
+    replays of the whole step (the programmatic launch of each attention kernel overlaps its prologue's tail), each
+    after an L2 flush outside the events.  Kernel times come from eager steps with CUDA events recorded around each
+    kernel; a GPU sleep before each eager step lets the host queue the whole step first, so that no launch waits for
+    the host inside the events.
+    """
+    stream = torch.cuda.current_stream()
+    layers = []
+    for li, W in enumerate(wl.windows):
+        q, k, v = (t.to(dev) for t in fwd_inputs(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D, seed=li if seeds is None else seeds[li]))
+        layers.append((q, k, v, torch.empty_like(q), W))
+    flops_layer = [fwd_flops(wl.B, wl.T, wl.Hq, wl.D, W) for W in wl.windows]
+    flops_step = sum(flops_layer)
+    wsp = torch.empty(nc.nc_attn_fwd_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D), dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        for li, (q, k, v, o, W) in enumerate(layers):
+            nc.nc_attn_fwd(q, k, v, o, window=W, workspace=wsp, events=evs[li] if evs else None)
+
+    for _ in range(max(3, n_warmup)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    for _ in range(max(3, n_warmup)):
+        flush.fill_(1)
+        g_step.replay()
+    torch.cuda.synchronize()
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    step_ev = [(mk(), mk()) for _ in range(n_steps)]
+    for s_ in range(n_steps):
+        flush.fill_(s_ & 0xFF)
+        step_ev[s_][0].record(stream)
+        g_step.replay()
+        step_ev[s_][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+
+    # kernel times: events around each kernel in eager steps
+    n_k = max(3, min(n_steps, 30))
+    k_ev = [[(mk(), mk(), mk()) for _ in layers] for _ in range(n_k)]
+    for s_ in range(n_k):
+        flush.fill_(s_ & 0xFF)
+        torch.cuda._sleep(2_000_000)            # ~1 ms at 2 GHz: the host queues the step meanwhile
+        step(k_ev[s_])
+    torch.cuda.synchronize()
+    per_w = {}
+    k2_tot_ms = 0.0
+    k1_tot_ms = 0.0
+    for li, (q, k, v, o, W) in enumerate(layers):
+        k2 = [row[li][1].elapsed_time(row[li][2]) for row in k_ev]
+        k1 = [row[li][0].elapsed_time(row[li][1]) for row in k_ev]
+        k2_tot_ms += sum(k2)
+        k1_tot_ms += sum(k1)
+        us = 1e3 * statistics.mean(k2)
+        key = str(W) if str(W) not in per_w else f"{W}#{li}"
+        per_w[key] = {"attn_us_per_launch": us, "attn_tflops": flops_layer[li] / (us * 1e-6) / 1e12,
+                      "prologue_us_per_launch": 1e3 * statistics.mean(k1)}
+    pro_bytes = prologue_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D)
+    pro_us = 1e3 * k1_tot_ms / (n_k * len(layers))
+    attn_achieved = n_k * flops_step / (k2_tot_ms * 1e-3) / 1e12
+    sec = {
+        "workload": f"{wl.name}: B={wl.B} T={wl.T} Hq={wl.Hq} Hkv={wl.Hkv} D={wl.D}, windows {list(wl.windows)}",
+        "flops_per_step": flops_step,
+        "us_per_step": 1e3 * statistics.mean(step_ms),
+        "tflops": n_steps * flops_step / (sum(step_ms) * 1e-3) / 1e12,
+        "attn_tflops": attn_achieved,
+        "attn_us_per_launch": 1e3 * k2_tot_ms / (n_k * len(layers)),
+        "prologue_us_per_launch": pro_us,
+        "prologue_gbs": pro_bytes / (pro_us * 1e-6) / 1e9,
+        "prologue_bytes_per_launch": pro_bytes,
+        "windows": per_w,
+        "steps_timed": n_steps, "kernel_steps_timed": n_k,
+    }
+    return sec, step_ms, layers, wsp
+
+
 def run_ours(args, ws, rank, local):
     from transformer_attention_06_b300 import nc_attn as nc
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    w = DEPTH12
-    layers = []
-    for li, W in enumerate(w.windows):
-        q, k, v = (t.to(dev) for t in fwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=li))
-        layers.append((q, k, v, torch.empty_like(q), W))
-    flops_layer = [fwd_flops(w.B, w.T, w.Hq, w.D, W) for W in w.windows]
-    flops_step = sum(flops_layer)
-    wsp = torch.empty(nc.nc_attn_fwd_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step(evs=None):
-        for li, (q, k, v, o, W) in enumerate(layers):
-            nc.nc_attn_fwd(q, k, v, o, window=W, workspace=wsp, events=evs[li] if evs else None)
-
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    # One step (the four layer calls) captured once as a CUDA graph and replayed per timed step: the device work is
-    # the same as an eager step without the host launch gaps between the eight kernels.
-    g_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step):
-        step()
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        g_step.replay()
-    torch.cuda.synchronize()
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    step_ev = [(mk(), mk()) for _ in range(args.steps)]
+
+    def add_fracs(sec):
+        sec["frac"] = sec["tflops"] / peaks["bf16_tflops"]
+        sec["attn_frac"] = sec["attn_tflops"] / peaks["bf16_tflops"]
+        sec["attn_frac_of_sustained"] = sec["attn_tflops"] / peaks["bf16_tflops_sustained"]
+        sec["prologue_frac_of_hbm"] = sec["prologue_gbs"] / peaks["hbm_gbs"]
+        for d in sec["windows"].values():
+            d["attn_frac"] = d["attn_tflops"] / peaks["bf16_tflops"]
+        return sec
+
+    # ---- headline: the long-context step, with clocks sampled during its timed region
+    w = LONG
     clocks = ClockSampler(local)
     clocks.start()
     dist_barrier(ws)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for s in range(args.steps):
-        flush.fill_(s & 0xFF)
-        step_ev[s][0].record(stream)
-        g_step.replay()
-        step_ev[s][1].record(stream)
+    head, step_ms, layers, wsp = prefill_section(nc, w, dev, flush, args.steps, args.warmup)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     clk = clocks.stop(t_wall0, t_wall1)
     dist_barrier(ws)
-    total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
-    total_ms_max = dist_max(total_ms, ws)
+    add_fracs(head)
+    flops_step = head["flops_per_step"]
+    total_ms_max = dist_max(sum(step_ms), ws)
     value = ws * args.steps * flops_step / (total_ms_max * 1e-3) / 1e12
-
-    # Kernel times for the roofline: eager steps with CUDA events recorded on the stream around each kernel.
-    n_roof = min(args.steps, 50)
-    k_ev = [[(mk(), mk(), mk()) for _ in layers] for _ in range(n_roof)]
-    for s in range(n_roof):
-        flush.fill_(s & 0xFF)
-        step(k_ev[s])
-    torch.cuda.synchronize()
-    k2_ms = [[e[1].elapsed_time(e[2]) for e in row] for row in k_ev]
-    k1_ms = [[e[0].elapsed_time(e[1]) for e in row] for row in k_ev]
-    k2_total = sum(sum(r) for r in k2_ms)
-    k2_flops = n_roof * flops_step
-    achieved = k2_flops / (k2_total * 1e-3) / 1e12
     traffic = kernel_traffic("attn_fwd_kernel", ["transformer_attention_06_b300/csrc/attn_fwd.cuh",
                                                  "transformer_attention_06_b300/csrc/common.cuh"])
 
@@ -380,6 +448,18 @@ def run_ours(args, ws, rank, local):
         e2e_ms = dist_max(sum(times), ws)
         e2e = {"value": ws * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+        del host
+    del layers, wsp
+    torch.cuda.empty_cache()
+
+    # ---- the other prefill workloads, one section each (the long-context section is the headline's)
+    prefill = {LONG.name: head}
+    if not args.skip_sections:
+        for wl in (TINY, DEPTH12, GQA):
+            sec, _, lay, wsp_ = prefill_section(nc, wl, dev, flush, 20)
+            prefill[wl.name] = add_fracs(sec)
+            del lay, wsp_
+            torch.cuda.empty_cache()
 
     # ---- decode
     dec = None
@@ -475,6 +555,7 @@ def run_ours(args, ws, rank, local):
     # ---- backward pass (CUDA-core kernels) on the depth-12 layer shapes
     bwd = None
     if not args.skip_decode:
+        w = DEPTH12
         bq, bk, bv, bdo = (t.to(dev) for t in bwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=0))
         bws = torch.empty(int(nc.lib.nc_attn_bwd_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D)), dtype=torch.uint8,
                           device=dev)
@@ -511,28 +592,30 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{w.name}: B={w.B} T={w.T} Hq={w.Hq} Hkv={w.Hkv} D={w.D}, one step = SSSL "
-                                   f"layers with windows {list(w.windows)}, distinct seeded q,k,v per layer",
+            "config": {"workload": LONG_WORKLOAD,
                        "l2": "512 MiB write before every timed step, outside the timed events",
-                       "timing": "each step replayed from a CUDA graph of its eight kernels; kernel times for the "
+                       "timing": "each step replayed from a CUDA graph of its four kernels; kernel times for the "
                                  "roofline from CUDA events around each kernel in eager steps",
                        "flops_per_step": flops_step, "parallelism": f"replicas x{ws}"},
             "frac_of_bf16_peak": value / ws / peaks["bf16_tflops"],
-            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved,
-                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                         "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": head["attn_tflops"],
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": head["attn_frac"],
+                         "frac_of_sustained": head["attn_frac_of_sustained"],
                          "traffic": traffic, "peak_source": f"{peak_src} bf16 dense (burst)",
                          "achieved_def": "sum of in-band FLOPs of the attention-kernel launches / sum of their "
-                                         "CUDA-event durations",
-                         "us_per_launch": 1e3 * k2_total / (n_roof * len(layers)),
-                         "prologue_us_per_launch": 1e3 * sum(sum(r) for r in k1_ms) / (n_roof * len(layers)),
-                         "launches_timed": n_roof * len(layers)},
+                                         "CUDA-event durations, on the long-context step",
+                         "us_per_launch": head["attn_us_per_launch"],
+                         "launches_timed": head["kernel_steps_timed"] * len(LONG.windows),
+                         "prologue": {"bound": "hbm", "us_per_launch": head["prologue_us_per_launch"],
+                                      "achieved_gbs": head["prologue_gbs"], "peak_gbs": peaks["hbm_gbs"],
+                                      "frac": head["prologue_frac_of_hbm"]}},
+            "prefill": prefill,
             "decode": dec,
             "prefill_chunk": chk,
             "backward": bwd,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": args.steps * len(layers) * 2,
+            "gpu_launches": args.steps * len(LONG.windows) * 2,
             "clocks": clk,
             "device_status": nc.status_string(st),
         }
@@ -548,6 +631,7 @@ def main():
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-sections", action="store_true", help="time only the headline step (and decode etc.)")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":

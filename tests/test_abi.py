@@ -65,6 +65,10 @@ def test_fwd_rejects_bad_arguments(nc):
     assert fwd(nc, D=64) == U
     assert fwd(nc, T=1 << 24) == U
     assert fwd(nc, B=1 << 20, T=1 << 12) == U      # B * T tokens beyond 32-bit indexing
+    # the prologue rounds B * T up to its 32-token blocks in 32-bit arithmetic: 2^31 - 1 - 32 tokens is the largest
+    # accepted count (the call then fails only for want of a workspace), one more is refused
+    assert fwd(nc, B=155, T=13854733) == WS         # 2147483615 tokens
+    assert fwd(nc, B=87392, T=24573) == U           # 2147483616 tokens
     assert fwd(nc, Hq=256, Hkv=1) == U          # group larger than one 128-row tile
     assert fwd(nc) == WS                        # no workspace
     need = nc.nc_attn_fwd_workspace_bytes(1, 256, 4, 2)

@@ -65,3 +65,15 @@ def test_bwd_full_size_is_finite_and_linear(nc):
     for a, b in zip(g1, g2):
         assert torch.isfinite(a).all()
         torch.testing.assert_close(b, 2 * a, rtol=1e-5, atol=1e-6)
+
+
+def test_bwd_depth12_layer_one_sequence_matches_oracle(nc):
+    """The depth-12 layer shapes (T=2048, Hq=Hkv=6, window 1024) on one sequence, every gradient element against the
+    dense oracle."""
+    q, k, v, dout = bwd_inputs(1, 2048, 6, 6, 128, seed=0)
+    dq, dk, dv = nc.nc_attn_bwd(q.cuda(), k.cuda(), v.cuda(), dout.cuda(), window=1024)
+    torch.cuda.synchronize()
+    _, rq, rk, rv = backward.attn_fwd_bwd(f64(q), f64(k), f64(v), f64(dout), 1024)
+    check(dq, rq, "dq depth-12 layer")
+    check(dk, rk, "dk depth-12 layer")
+    check(dv, rv, "dv depth-12 layer")

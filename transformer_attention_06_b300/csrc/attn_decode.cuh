@@ -791,24 +791,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           finish = *last_flag != 0;
           if (finish) {
-            // Online log-sum-exp merge over the parts; the loads of one part are independent of each other.
-            if (!self_in_regs) {
+            // Online log-sum-exp merge over the parts, always in part order (whichever CTA arrives last merges), so
+            // that the result does not depend on the arrival order.  The loads of one part are independent of each
+            // other; this CTA's own part comes from registers when it did not publish it.
+            float own_m[G], own_l[G], own_o[G];
 #pragma unroll
-              for (int j = 0; j < G; ++j) {
-                M[j] = -INFINITY;
-                L[j] = 0.f;
-                o[j] = 0.f;
-              }
+            for (int j = 0; j < G; ++j) {
+              own_m[j] = M[j];
+              own_l[j] = L[j];
+              own_o[j] = o[j];
+              M[j] = -INFINITY;
+              L[j] = 0.f;
+              o[j] = 0.f;
             }
             for (int k = 0; k <= c_last - c_first; ++k) {
               const int sl = part_slot[k];
-              if (sl < 0 || (self_in_regs && sl == my_slot)) continue;
+              if (sl < 0) continue;
+              const bool own = self_in_regs && sl == my_slot;
               float pm[G], pl[G], po[G];
 #pragma unroll
               for (int j = 0; j < G; ++j) {
-                pm[j] = __ldcg(p.ws_ml + (static_cast<size_t>(sl) + j) * 2);
-                pl[j] = __ldcg(p.ws_ml + (static_cast<size_t>(sl) + j) * 2 + 1);
-                po[j] = __ldcg(p.ws_o + (static_cast<size_t>(sl) + j) * 128 + r);
+                pm[j] = own ? own_m[j] : __ldcg(p.ws_ml + (static_cast<size_t>(sl) + j) * 2);
+                pl[j] = own ? own_l[j] : __ldcg(p.ws_ml + (static_cast<size_t>(sl) + j) * 2 + 1);
+                po[j] = own ? own_o[j] : __ldcg(p.ws_o + (static_cast<size_t>(sl) + j) * 128 + r);
               }
 #pragma unroll
               for (int j = 0; j < G; ++j) {

@@ -86,7 +86,8 @@ nc_status check_fwd_shapes(int B, int T, int Hq, int Hkv, int D) {
   if (Hq % Hkv != 0) return NC_ERR_INVALID_ARG;
   if (D != 128) return NC_ERR_UNSUPPORTED;
   if (T >= (1 << 24)) return NC_ERR_UNSUPPORTED;  // positions must be exact in fp32
-  if (static_cast<long long>(B) * T > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;  // token index in 32 bits
+  // Token indices are 32-bit in the prologue kernels, including the block rounding of the token count.
+  if (static_cast<long long>(B) * T > 0x7fffffffLL - nc::kPrologueTokensPerBlock) return NC_ERR_UNSUPPORTED;
   const long double elems = static_cast<long double>(B) * T * Hq * D;
   if (elems > 9.0e15L) return NC_ERR_INVALID_ARG;
   return NC_OK;
