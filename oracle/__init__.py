@@ -11,6 +11,10 @@ Modules:
                computed.  The reference for every parity test.
 * ``brute`` -- scalar Python loops with an explicit full score matrix and mask.  Tiny inputs only; it pins
                ``ref`` (brute force on tiny inputs).
+* ``fp8``   -- the prefill forward with its score contraction on e4m3 operands (per-tensor scales fixed by the
+               QK-norm); pinned by the e4m3 code table, exhaustive nearest search, torch's float8 cast and
+               brute force (``tests/test_oracle_fp8.py``).
+* ``backward`` -- the chain rule of the block in fp64; pinned by central finite differences.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py`` (closed forms, brute force,
 invariants), except two documented readings that no page decides: the sign of the RoPE rotation and the

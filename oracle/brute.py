@@ -87,3 +87,56 @@ def attn_decode_brute(q, kcache, vcache, cache_lens, window, k_new=None, v_new=N
             for d in range(D):
                 out[b][h][d] = sum(e[j] / z * vals[j][g][d] for j in vis)
     return out
+
+
+def _e4m3_values():
+    """Every finite float8_e4m3fn value with its code, from the bit layout: sign, 4 exponent bits (bias 7), 3 mantissa
+    bits; exponent field 0 holds the subnormals m * 2^-9; S.1111.111 is NaN."""
+    vals = []
+    for code in range(256):
+        e, m = (code >> 3) & 0xF, code & 7
+        if e == 0xF and m == 7:
+            continue
+        mag = m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        vals.append((-mag if code & 0x80 else mag, code))
+    return vals
+
+
+_E4M3 = _e4m3_values()
+
+
+def e4m3_nearest(x):
+    """Nearest finite e4m3 value to x by exhaustive search; on a tie the value whose mantissa (lowest code bit) is
+    even."""
+    best = None
+    for val, code in _E4M3:
+        d = abs(val - x)
+        if best is None or d < best[0] or (d == best[0] and (code & 1) == 0 and (best[2] & 1) == 1):
+            best = (d, val, code)
+    return best[1]
+
+
+def attn_fwd_fp8_brute(q, k, v, window, s_q, s_k, rope_base=100000.0, eps=1e-6):
+    """Scalar version of the fp8 prefill: qn * s_q and kn * s_k rounded to e4m3 element by element (exhaustive
+    nearest search), the full score matrix of the quantised vectors divided by s_q s_k and scaled by 1 / sqrt(D), an
+    explicit mask and softmax, values as given."""
+    B, T, Hq, D, Hkv = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0]), len(k[0][0])
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(D)
+    out = [[[[0.0] * D for _ in range(Hq)] for _ in range(T)] for _ in range(B)]
+    for b in range(B):
+        qn = [[[e4m3_nearest(x * s_q) for x in _rope_norm_vec(q[b][t][h], t, rope_base, eps)] for h in range(Hq)]
+              for t in range(T)]
+        kn = [[[e4m3_nearest(x * s_k) for x in _rope_norm_vec(k[b][t][g], t, rope_base, eps)] for g in range(Hkv)]
+              for t in range(T)]
+        for h in range(Hq):
+            g = h // G
+            for i in range(T):
+                vis = [j for j in range(T) if j <= i and (window < 0 or i - j <= window)]
+                s = {j: sum(qn[i][h][d] * kn[j][g][d] for d in range(D)) / (s_q * s_k) * scale for j in vis}
+                mx = max(s.values())
+                e = {j: math.exp(s[j] - mx) for j in vis}
+                z = sum(e.values())
+                for d in range(D):
+                    out[b][i][h][d] = sum(e[j] / z * float(v[b][j][g][d]) for j in vis)
+    return out
