@@ -243,9 +243,10 @@ def dist_barrier(ws):
 
 
 # ------------------------------------------------------------------------------------------------- CPU (oracle)
-def prologue_bytes(B, T, Hq, Hkv, D):
-    """Algorithmic HBM bytes of the RoPE + QK-norm prologue: read q and k, write qn and kn (bf16)."""
-    return 2 * 2 * B * T * (Hq + Hkv) * D
+def prologue_bytes(B, T, Hq, Hkv, D, out_bytes=2):
+    """Algorithmic HBM bytes of the RoPE + QK-norm prologue: read q and k (bf16), write qn and kn (bf16, or e4m3 with
+    out_bytes=1)."""
+    return (2 + out_bytes) * B * T * (Hq + Hkv) * D
 
 
 def oracle_fwd_sample(wl, W, batches, groups=None):
@@ -303,7 +304,7 @@ LONG_WORKLOAD = (f"{LONG.name}: B={LONG.B} T={LONG.T} Hq={LONG.Hq} Hkv={LONG.Hkv
 
 
 # ---------------------------------------------------------------------------------------------------- GPU arm
-def prefill_section(nc, wl, dev, flush, n_steps, n_warmup=3, seeds=None):
+def prefill_section(nc, wl, dev, flush, n_steps, n_warmup=3, seeds=None, fp8=False):
     """Times one prefill workload: a step is one call per window of `wl` (call i on inputs of seed i, or seeds[i]).
 
     Returns (section dict, per-step event times in ms, layer tensors, workspace).  The step time comes from CUDA-graph
@@ -319,11 +320,14 @@ def prefill_section(nc, wl, dev, flush, n_steps, n_warmup=3, seeds=None):
         layers.append((q, k, v, torch.empty_like(q), W))
     flops_layer = [fwd_flops(wl.B, wl.T, wl.Hq, wl.D, W) for W in wl.windows]
     flops_step = sum(flops_layer)
-    wsp = torch.empty(nc.nc_attn_fwd_workspace_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D), dtype=torch.uint8, device=dev)
+    ws_bytes = (nc.nc_attn_fwd_fp8_workspace_bytes if fp8 else nc.nc_attn_fwd_workspace_bytes)(
+        wl.B, wl.T, wl.Hq, wl.Hkv, wl.D)
+    wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    fwd = nc.nc_attn_fwd_fp8 if fp8 else nc.nc_attn_fwd
 
     def step(evs=None):
         for li, (q, k, v, o, W) in enumerate(layers):
-            nc.nc_attn_fwd(q, k, v, o, window=W, workspace=wsp, events=evs[li] if evs else None)
+            fwd(q, k, v, o, window=W, workspace=wsp, events=evs[li] if evs else None)
 
     for _ in range(max(3, n_warmup)):
         flush.fill_(1)
@@ -366,7 +370,7 @@ def prefill_section(nc, wl, dev, flush, n_steps, n_warmup=3, seeds=None):
         key = str(W) if str(W) not in per_w else f"{W}#{li}"
         per_w[key] = {"attn_us_per_launch": us, "attn_tflops": flops_layer[li] / (us * 1e-6) / 1e12,
                       "prologue_us_per_launch": 1e3 * statistics.mean(k1)}
-    pro_bytes = prologue_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D)
+    pro_bytes = prologue_bytes(wl.B, wl.T, wl.Hq, wl.Hkv, wl.D, out_bytes=1 if fp8 else 2)
     pro_us = 1e3 * k1_tot_ms / (n_k * len(layers))
     attn_achieved = n_k * flops_step / (k2_tot_ms * 1e-3) / 1e12
     sec = {
@@ -460,6 +464,25 @@ def run_ours(args, ws, rank, local):
             prefill[wl.name] = add_fracs(sec)
             del lay, wsp_
             torch.cuda.empty_cache()
+
+    # ---- the prefill with e4m3 score operands: half of the in-band FLOPs (Q K^T) on the 8-bit tensor path at twice the
+    # bf16 rate, the other half (P V) in bf16, so its peak is 4/3 of the bf16 peak
+    prefill_fp8 = None
+    if not args.skip_sections:
+        prefill_fp8 = {}
+        peak8 = peaks["bf16_tflops"] * 4.0 / 3.0
+        for wl in (LONG, GQA, DEPTH12):
+            sec, _, lay, wsp_ = prefill_section(nc, wl, dev, flush, 20, fp8=True)
+            for d in [sec] + list(sec["windows"].values()):
+                d["attn_frac"] = d["attn_tflops"] / peak8
+            sec["frac"] = sec["tflops"] / peak8
+            sec["prologue_frac_of_hbm"] = sec["prologue_gbs"] / peaks["hbm_gbs"]
+            prefill_fp8[wl.name] = sec
+            del lay, wsp_
+            torch.cuda.empty_cache()
+        prefill_fp8["peak_tflops"] = peak8
+        prefill_fp8["peak_def"] = ("QK^T (half the in-band FLOPs) on e4m3 at 2x the bf16 rate, P V in bf16: 4/3 of the "
+                                   "measured bf16 dense peak (the nominal fp8 : bf16 ratio is 2)")
 
     # ---- decode
     dec = None
@@ -610,6 +633,7 @@ def run_ours(args, ws, rank, local):
                                       "achieved_gbs": head["prologue_gbs"], "peak_gbs": peaks["hbm_gbs"],
                                       "frac": head["prologue_frac_of_hbm"]}},
             "prefill": prefill,
+            "prefill_fp8": prefill_fp8,
             "decode": dec,
             "prefill_chunk": chk,
             "backward": bwd,

@@ -12,7 +12,8 @@
  *   - "nanochat (Fucina port)", section "Architecture": half-split RoPE with an inverse-built table,
  *     no-weight RMSNorm, grouped causal attention.
  *
- * Entry points: the prefill forward (nc_attn_fwd*), the chunked prefill against a KV cache (nc_attn_prefill_chunk*),
+ * Entry points: the prefill forward (nc_attn_fwd*; nc_attn_fwd_fp8* with e4m3 score operands), the chunked prefill
+ * against a KV cache (nc_attn_prefill_chunk*),
  * the single-token decode (nc_attn_decode*), the same three with a QK-norm gain on the logits (*_ex), the backward
  * pass of the prefill (nc_attn_bwd_ws), the RoPE + norm kernel alone (nc_attn_qk_prologue), and status helpers.
  *
@@ -89,6 +90,37 @@ nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, voi
  */
 nc_status nc_attn_qk_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
                               int D, float rope_base, cudaStream_t stream);
+
+/* ---- prefill forward with e4m3 (fp8) score operands -----------------------------------------------------------
+ * ("nanochat Admin & Developer Guide", section 6: the fast attention kernel takes bf16 or fp8 operands; section 5
+ * "Precision", FP8 training: operands of a product quantised to float8_e4m3fn with one scale per tensor, fp32
+ * accumulation, the scales removed from the result.)  Same inputs, output, positions, window and grouping as
+ * nc_attn_fwd_ex (qk_gain in (0, 4] multiplies every logit).  The difference: the roped + normed qn and kn are
+ * rounded to e4m3 as qn * s_q and kn * s_k, with s_q = 4 qk_gain log2(e) / sqrt(D) and s_k = 1/4 (unit-RMS vectors
+ * bound every element by sqrt(D), so these fixed per-tensor scales keep both inside e4m3's +-448), and the score
+ * contraction runs on the tensor cores' 8-bit path; its result divided by s_q s_k and times qk_gain / sqrt(D) is the
+ * logit.  The probabilities and v stay bf16 (P.V in bf16 with fp32 accumulation), the output is bf16.
+ *
+ * workspace: caller-owned device memory of at least nc_attn_fwd_fp8_workspace_bytes(...) bytes, 16-byte aligned,
+ * no initial contents required (the e4m3 qn and kn and a counter); not to be shared by calls that overlap on the GPU.
+ * nc_attn_fwd_fp8_events additionally records `k1_begin`, `k2_begin`, `k2_end` around the two kernels it launches
+ * (any may be NULL), as nc_attn_fwd_ws_events does.
+ * nc_attn_qk_prologue_fp8 runs the first kernel alone: qn8 [B,T,Hq,D] and kn8 [B,T,Hkv,D] receive the e4m3 codes
+ * (one byte per element, round to nearest even) of qn * s_q and kn * s_k.
+ */
+size_t nc_attn_fwd_fp8_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
+
+nc_status nc_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                          int D, int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+nc_status nc_attn_fwd_fp8_events(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,
+                                 int Hkv, int D, int window, float rope_base, float qk_gain, void* workspace,
+                                 size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin,
+                                 cudaEvent_t k2_end, cudaStream_t stream);
+
+nc_status nc_attn_qk_prologue_fp8(const void* q, const void* k, void* qn8, void* kn8, int B, int T, int Hq, int Hkv,
+                                  int D, float rope_base, float qk_gain, cudaStream_t stream);
 
 /* ---- Chunked prefill against a KV cache ------------------------------------------------------------------------
  * ("nanochat Admin & Developer Guide", section 6: the SDPA fallback's third case, chunked / sliding-window

@@ -235,3 +235,26 @@ def test_a_c_program_links_and_calls_the_library(tmp_path):
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
     assert int(out[0]) == nc_attn.nc_attn_fwd_workspace_bytes(4, 2048, 6, 6)
     assert int(out[1]) == nc_attn.NC_ERR_INVALID_ARG
+
+
+def test_fwd_fp8_rejects_bad_arguments(nc):
+    E, U, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_UNSUPPORTED, nc.NC_ERR_WORKSPACE
+    f = nc.lib.nc_attn_fwd_fp8
+
+    def call(q=P, k=P, v=P, out=P, B=1, T=256, Hq=4, Hkv=2, D=128, W=-1, base=1e5, gain=1.0, ws=None, wsb=0):
+        return f(q, k, v, out, B, T, Hq, Hkv, D, W, base, gain, ws, wsb, None)
+
+    assert call(q=None) == E
+    assert call(v=PM) == E
+    assert call(Hq=3, Hkv=2) == E
+    assert call(W=-2) == E
+    assert call(gain=0.0) == E and call(gain=4.5) == E
+    assert call(D=64) == U
+    assert call() == WS
+    need = nc.lib.nc_attn_fwd_fp8_workspace_bytes(1, 256, 4, 2, 128)
+    assert need == 256 * (4 + 2) * 128 + 256          # one byte per element of qn and kn, then the counter
+    assert call(ws=P, wsb=need - 1) == WS
+    g = nc.lib.nc_attn_qk_prologue_fp8
+    assert g(None, P, P, P, 1, 8, 2, 2, 128, 1e5, 1.0, None) == E
+    assert g(P, P, P, P, 1, 8, 2, 2, 128, 1e5, 5.0, None) == E
+    assert g(P, P, P, P, 1, 8, 2, 2, 96, 1e5, 1.0, None) == U

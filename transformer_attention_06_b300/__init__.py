@@ -10,6 +10,7 @@ _EXPORTS = (
     "nc_attn_decode",
     "nc_attn_decode_workspace_bytes",
     "nc_attn_fwd",
+    "nc_attn_fwd_fp8",
     "nc_attn_fwd_workspace_bytes",
     "nc_attn_get_device_status",
     "nc_attn_qk_prologue",

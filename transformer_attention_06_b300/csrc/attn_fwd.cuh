@@ -60,6 +60,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                 // S_X at kColS + 128 X
 constexpr uint32_t kColO = 256;               // O_X at kColO + 128 X
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);  // A = Q, B = K, both K-major
+constexpr uint32_t kIdescQK8 = idesc_e4m3_f32(128, 128);                // the same with e4m3 Q and K
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // A = P (TMEM), B = V (MN-major)
 // Softmax without a running maximum.  kn and qn are RMS-normalised by the prologue (RMSNorm without weight,
 // eps > 0), and qn leaves it multiplied by c = g log2(e) / sqrt(128) (g: the QK-norm gain, 1 or e.g. 1.2, at most
@@ -69,11 +70,6 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // A = P 
 // so the exponentials need no offset and neither O nor the row sums ever need rescaling; softmax(x) =
 // 2^S / sum 2^S exactly as with a maximum.
 
-constexpr int kOffQ = 0;                                 // Q_A, Q_B
-constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffO = kOffV + kVStages * kTileBytes;    // output staging of one Q tile (TMA store source)
-constexpr int kOffBar = kOffO + kTileBytes;
 // mbarrier slots (each 8 bytes), derived from the ring depths so that no two barriers can overlap.
 constexpr int kBarKFull = 0;
 constexpr int kBarKEmpty = kBarKFull + kKStages;
@@ -90,13 +86,27 @@ constexpr int kBarSchedEmpty = kBarSchedFull + 2;
 constexpr int kBarMmaFinal = kBarSchedEmpty + 2;   // [2], one per MMA warp
 constexpr int kNumBars = kBarMmaFinal + 2;
 static_assert(kNumBars <= 32, "barrier block");
-constexpr int kOffXch = kOffBar + kNumBars * 8;  // row-sum exchange, [2 halves][128] f32 (1 KB used)
-constexpr int kOffMisc = kOffXch + 2048;
 // The dynamic shared memory base is aligned up to 1024 bytes inside the kernel; 768 bytes of slack cover bases
 // that are at least 256-byte aligned (in practice it is 1024-byte aligned), and the kernel checks this.
 constexpr int kAlignSlack = 768;
-constexpr int kSmemBytes = kOffMisc + 16 + kAlignSlack;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Shared-memory layout.  Q and K tiles hold 128 rows of 128 elements: 32 KB in bf16 (two 64-column halves of 128
+// bytes per row), 16 KB in e4m3 (one 128-byte row each).  V and the output staging tile are bf16 in both variants.
+template <bool kFp8>
+struct Smem {
+  static constexpr int kQKBytes = kFp8 ? 128 * 128 : kTileBytes;  // one Q or K tile
+  static constexpr int kOffQ = 0;                                  // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kQKBytes;
+  static constexpr int kOffV = kOffK + kKStages * kQKBytes;
+  static constexpr int kOffO = kOffV + kVStages * kTileBytes;      // output staging of one Q tile (TMA store source)
+  static constexpr int kOffBar = kOffO + kTileBytes;
+  static constexpr int kOffXch = kOffBar + kNumBars * 8;           // row-sum exchange, [2 halves][128] f32 (1 KB used)
+  static constexpr int kOffMisc = kOffXch + 2048;
+  static constexpr int kBytes = kOffMisc + 16 + kAlignSlack;
+  static_assert(kBytes <= 232448, "shared memory budget");
+};
+constexpr int kSmemBytes = Smem<false>::kBytes;
+constexpr int kSmemBytesFp8 = Smem<true>::kBytes;
 
 struct Params {
   __nv_bfloat16* out;
@@ -164,17 +174,20 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item) {
   return it;
 }
 
+// kFp8: qn and kn are e4m3 (scores on tcgen05 kind::f8f6f4); otherwise bf16 (kind::f16).  P and V are bf16 in both.
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmVt,
                     const __grid_constant__ CUtensorMap tmO, const Params p) {
+  using L = Smem<kFp8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = smem + kOffQ;
-  uint8_t* sK = smem + kOffK;
-  uint8_t* sV = smem + kOffV;
-  uint8_t* sO = smem + kOffO;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint8_t* sQ = smem + L::kOffQ;
+  uint8_t* sK = smem + L::kOffK;
+  uint8_t* sV = smem + L::kOffV;
+  uint8_t* sO = smem + L::kOffO;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* k_full = bars + kBarKFull;        // [kKStages]  TMA -> MMA
   uint64_t* k_empty = bars + kBarKEmpty;      // [kKStages]  MMA -> TMA
   uint64_t* v_full = bars + kBarVFull;        // [kVStages]  TMA -> MMA
@@ -188,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sched_full = bars + kBarSchedFull;    // [2]  work item published                     TMA -> all
   uint64_t* sched_empty = bars + kBarSchedEmpty;  // [2]  work item read (2 MMA warps + the softmax warps)
   uint64_t* mma_final = bars + kBarMmaFinal;
-  float* xch = reinterpret_cast<float*>(smem + kOffXch);
-  int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+  float* xch = reinterpret_cast<float*>(smem + L::kOffXch);
+  int* misc = reinterpret_cast<int*>(smem + L::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = misc + 1;
   int* sched = misc + 2;            // [2] work-item ring
@@ -234,11 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Rows of the Q tiles that TMA never fills (128 is not a multiple of G): zero them once so they stay finite.
     const int x = threadIdx.x >> 7, r = threadIdx.x & 127;
     if (r >= p.G * p.P) {
-      uint4* r0 = reinterpret_cast<uint4*>(sQ + x * kTileBytes + r * 128);
-      uint4* r1 = reinterpret_cast<uint4*>(sQ + x * kTileBytes + kHalfBytes + r * 128);
-      for (int i = 0; i < 8; ++i) {
-        r0[i] = make_uint4(0, 0, 0, 0);
-        r1[i] = make_uint4(0, 0, 0, 0);
+      uint4* r0 = reinterpret_cast<uint4*>(sQ + x * L::kQKBytes + r * 128);
+      for (int i = 0; i < 8; ++i) r0[i] = make_uint4(0, 0, 0, 0);
+      if (!kFp8) {
+        uint4* r1 = reinterpret_cast<uint4*>(sQ + x * L::kQKBytes + kHalfBytes + r * 128);
+        for (int i = 0; i < 8; ++i) r1[i] = make_uint4(0, 0, 0, 0);
       }
     }
   }
@@ -250,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Everything above ran concurrently with the tail of the prologue kernel; qn, kn and the work counter are read
   // only after it has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const uint32_t q_bytes = 2u * 128u * static_cast<uint32_t>(p.G * p.P);  // one Q tile (box {64, G, P, 1} x 2)
+  // one Q tile: box {64, G, P, 1} x 2 in bf16, {128, G, P, 1} in e4m3
+  const uint32_t q_bytes = (kFp8 ? 1u : 2u) * 128u * static_cast<uint32_t>(p.G * p.P);
   if (warp >= 8) {
     warpgroup_reg_dec<kRegsOther>();
     if (warp == kProducerWarp && lane == 0) {
@@ -292,12 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Q tiles of item iq, once every S of item iq - 1 has completed
         if (iq < nfetched && (iq == 0 || mbar_test(q_empty, (iq - 1) & 1))) {
           const Item& it = items[iq & 1];
-          mbar_arrive_expect_tx(q_full + 0, q_bytes);
-          tma_load_4d(sQ, &tmQ, q_full + 0, 0, it.g * p.G, it.qa.t0, it.b);
-          tma_load_4d(sQ + kHalfBytes, &tmQ, q_full + 0, 64, it.g * p.G, it.qa.t0, it.b);
-          mbar_arrive_expect_tx(q_full + 1, q_bytes);  // past T the box reads as zeros (still full bytes)
-          tma_load_4d(sQ + kTileBytes, &tmQ, q_full + 1, 0, it.g * p.G, it.qb.t0, it.b);
-          tma_load_4d(sQ + kTileBytes + kHalfBytes, &tmQ, q_full + 1, 64, it.g * p.G, it.qb.t0, it.b);
+          // past T the box reads as zeros (still full bytes)
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int t0 = x == 0 ? it.qa.t0 : it.qb.t0;
+            mbar_arrive_expect_tx(q_full + x, q_bytes);
+            tma_load_4d(sQ + x * L::kQKBytes, &tmQ, q_full + x, 0, it.g * p.G, t0, it.b);
+            if (!kFp8) tma_load_4d(sQ + x * L::kQKBytes + kHalfBytes, &tmQ, q_full + x, 64, it.g * p.G, t0, it.b);
+          }
           ++iq;
           progress = true;
         }
@@ -305,10 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ik < nfetched && (kt < kKStages || mbar_test(k_empty + kt % kKStages, ((kt / kKStages) - 1) & 1))) {
           const Item& it = items[ik & 1];
           const int st = kt % kKStages;
-          uint8_t* dk = sK + st * kTileBytes;
-          mbar_arrive_expect_tx(k_full + st, kTileBytes);
+          uint8_t* dk = sK + st * L::kQKBytes;
+          mbar_arrive_expect_tx(k_full + st, L::kQKBytes);
           tma_load_4d(dk, &tmK, k_full + st, 0, it.g, jk * kBlockN, it.b);
-          tma_load_4d(dk + kHalfBytes, &tmK, k_full + st, 64, it.g, jk * kBlockN, it.b);
+          if (!kFp8) tma_load_4d(dk + kHalfBytes, &tmK, k_full + st, 64, it.g, jk * kBlockN, it.b);
           ++kt;
           if (++jk > it.hi) ++ik;  // the next item's first tile is set when it is fetched
           progress = true;
@@ -368,17 +384,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int x = warp == kMmaWarp ? 0 : 1;
       const bool leader = lane == 0;
       const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      // Tiles are 32 KB apart: the descriptor of buffer i is the one of buffer 0 plus i * (32 KB >> 4).
-      constexpr uint64_t kTileDesc = kTileBytes >> 4;
-      const uint64_t dq = sdesc_sw128(aQ, 16, 1024) + x * kTileDesc, dk0 = sdesc_sw128(aK, 16, 1024);
+      // Buffers of one kind are equally spaced: the descriptor of buffer i is the one of buffer 0 plus i times the
+      // buffer size >> 4.
+      constexpr uint64_t kTileDesc = kTileBytes >> 4, kQKDesc = L::kQKBytes >> 4;
+      const uint64_t dq = sdesc_sw128(aQ, 16, 1024) + x * kQKDesc, dk0 = sdesc_sw128(aK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(aV, kHalfBytes, 1024);
       const uint32_t tS = tbase + kColS + x * 128, tO = tbase + kColO + x * 128;
       auto issue_s = [&](int st) {  // S_X = Q_X K^T (K from stage st)
         if (leader) {
+          if constexpr (kFp8) {
+            // four K = 32 steps of 32 bytes along the 128-byte rows (kind::f8f6f4)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-            umma_ss(tS, dq + off, dk0 + st * kTileDesc + off, kIdescQK, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ss_f8(tS, dq + kk * 2, dk0 + st * kQKDesc + kk * 2, kIdescQK8, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+              umma_ss(tS, dq + off, dk0 + st * kQKDesc + off, kIdescQK, kk > 0 ? 1u : 0u);
+            }
           }
           umma_commit(s_full + x);
         }

@@ -3,9 +3,10 @@
 // Thin inline-PTX wrappers for the Blackwell primitives the kernels are built from:
 //   * mbarrier       -- arrive / expect-tx / bounded parity wait;
 //   * TMA            -- cp.async.bulk.tensor tile loads (128-byte swizzle, no multicast);
-//   * tcgen05        -- TMEM alloc / dealloc, single-thread MMA issue (kind::f16, fp32 accumulate),
+//   * tcgen05        -- TMEM alloc / dealloc, single-thread MMA issue (kind::f16 and kind::f8f6f4, fp32
+//                       accumulate),
 //                       commit-to-mbarrier, and 32x32b TMEM loads / stores;
-//   * descriptors    -- the shared-memory matrix descriptor and the kind::f16 instruction descriptor,
+//   * descriptors    -- the shared-memory matrix descriptor and the kind::f16 / kind::f8f6f4 instruction descriptors,
 //                       built from the field tables of the PTX ISA (tcgen05 "Matrix Descriptors").
 //
 // Every wait is bounded: after `limit_ns` of global time a wait gives up, records NC_DEV_TIMEOUT in the
@@ -70,6 +71,15 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // .x (low 16 bits) = lo
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four fp32 values rounded to e4m3 (round to nearest even, saturating to +-448), packed with a0 in the lowest byte.
+// The conversion puts its first source operand in the upper byte of each 16-bit pair.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(lo) : "f"(a0), "f"(a1));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(hi) : "f"(a2), "f"(a3));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 // acc + lo + hi for the two bf16 halves of `pair` (exact widening, fp32 adds).
@@ -248,6 +258,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0 in bits 7-9 and 10-12), both K-major,
+// and an fp32 accumulator; the other fields as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ---- tcgen05: MMA issue and commit (one thread) ---------------------------------------------------------------
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -255,6 +272,15 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem], 8-bit operands (K = 32 per instruction)
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

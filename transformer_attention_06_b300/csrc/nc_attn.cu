@@ -42,19 +42,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A 4-D bf16 view [d3][d2][d1][d0] (d0 innermost, contiguous), 128-byte swizzle, zero fill out of bounds.
+// A 4-D view [d3][d2][d1][d0] (d0 innermost, contiguous) of bf16 elements (or of bytes when `bytes` is set: e4m3
+// codes), 128-byte swizzle, zero fill out of bounds.
 bool make_map_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
-                 uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+                 uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3, bool bytes = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
+  const uint64_t es = bytes ? 1 : 2;
   const cuuint64_t dims[4] = {d0, d1, d2, d3};
-  const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  const cuuint64_t strides[3] = {d0 * es, d0 * d1 * es, d0 * d1 * d2 * es};
   const cuuint32_t box[4] = {b0, b1, b2, b3};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   std::memset(map, 0, sizeof(*map));
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ---------------------------------------------------------------------------------------------------------------
@@ -70,6 +72,12 @@ RopeTable rope_table(float base) {
 }
 
 float scale_log2_for_d128() { return static_cast<float>(1.4426950408889634 / std::sqrt(128.0)); }
+
+// Per-tensor scales of the e4m3 qn and kn: s_q = 4 g log2(e) / sqrt(128) and s_k = 1/4.  Every element of a unit-RMS
+// vector lies within +-sqrt(128), so both stay far inside e4m3's +-448 for gains up to 4; their product makes the
+// e4m3 product a base-2 logit; the factors 4 and 1/4 keep typical elements of both operands in e4m3's normal range.
+constexpr float kFp8KScale = 0.25f;
+float fp8_q_scale(float qk_gain) { return 4.0f * scale_log2_for_d128() * qk_gain; }
 
 // Largest accepted gain on the logits.  The prefill kernel takes exponentials without a running maximum: with unit-RMS
 // qn, kn its base-2 logits are bounded by 16.5 times the gain, so a gain of at most 4 keeps 2^S within [2^-66, 2^66]
@@ -109,17 +117,25 @@ void set_smem_attr_once(F* kernel, int bytes, int slot) {
 
 nc_status launch_status() { return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA; }
 
+// fp8: qn, kn written as e4m3 codes times q_scale, k_scale (else bf16, kn unscaled).
 nc_status launch_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
                           const RopeTable& tab, float q_scale, unsigned* zero_word, cudaStream_t stream,
                           const void* v = nullptr, const void* ve = nullptr, const void* ve_gate = nullptr,
-                          void* vmix = nullptr) {
+                          void* vmix = nullptr, bool fp8 = false, float k_scale = 1.0f) {
   const int BT = B * T;
   const int blocks = (BT + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
-  nc::qk_prologue_kernel<<<blocks, nc::kPrologueThreads, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(qn),
-      static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, q_scale, zero_word,
-      static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(ve),
-      static_cast<const __nv_bfloat16*>(ve_gate), static_cast<__nv_bfloat16*>(vmix));
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  if (fp8) {
+    nc::qk_prologue_kernel<uint8_t><<<blocks, nc::kPrologueThreads, 0, stream>>>(
+        qb, kb, static_cast<uint8_t*>(qn), static_cast<uint8_t*>(kn), BT, T, Hq, Hkv, tab, q_scale, k_scale,
+        zero_word, nullptr, nullptr, nullptr, nullptr);
+  } else {
+    nc::qk_prologue_kernel<__nv_bfloat16><<<blocks, nc::kPrologueThreads, 0, stream>>>(
+        qb, kb, static_cast<__nv_bfloat16*>(qn), static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, q_scale,
+        k_scale, zero_word, static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(ve),
+        static_cast<const __nv_bfloat16*>(ve_gate), static_cast<__nv_bfloat16*>(vmix));
+  }
   return launch_status();
 }
 
@@ -229,8 +245,11 @@ nc_status check_decode_args(const void* q, const void* kcache, const void* vcach
 // may start (and set up barriers and TMEM) while the prologue drains; they wait on the prologue grid
 // (griddepcontrol.wait) before touching anything it writes.
 nc_status launch_attention(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mvt,
-                           const CUtensorMap& mo, const nc::fwd::Params& prm, int n_sm, cudaStream_t stream) {
-  set_smem_attr_once(nc::fwd::attn_fwd_kernel, nc::fwd::kSmemBytes, 0);
+                           const CUtensorMap& mo, const nc::fwd::Params& prm, int n_sm, cudaStream_t stream,
+                           bool fp8 = false) {
+  auto* kernel = fp8 ? nc::fwd::attn_fwd_kernel<true> : nc::fwd::attn_fwd_kernel<false>;
+  const int smem = fp8 ? nc::fwd::kSmemBytesFp8 : nc::fwd::kSmemBytes;
+  set_smem_attr_once(kernel, smem, fp8 ? 17 : 0);
   const int grid = std::min(n_sm, prm.n_items);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -238,11 +257,11 @@ nc_status launch_attention(const CUtensorMap& mq, const CUtensorMap& mk, const C
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(nc::fwd::kThreads);
-  cfg.dynamicSmemBytes = nc::fwd::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, nc::fwd::attn_fwd_kernel, mq, mk, mv, mvt, mo, prm) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mvt, mo, prm) != cudaSuccess) {
     (void)cudaGetLastError();  // clear it: the failure is reported here
     return NC_ERR_CUDA;
   }
@@ -292,7 +311,8 @@ nc_status nc_attn_fwd_ws(const void* q, const void* k, const void* v, void* out,
 static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
                           int D, int window, float rope_base, float qk_gain, void* workspace,
                           size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin, cudaEvent_t k2_end,
-                          cudaStream_t stream, const void* ve = nullptr, const void* ve_gate = nullptr) {
+                          cudaStream_t stream, const void* ve = nullptr, const void* ve_gate = nullptr,
+                          bool fp8 = false) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return NC_ERR_INVALID_ARG;
   if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NC_ERR_INVALID_ARG;
@@ -303,14 +323,17 @@ static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out
   if (!fwd_split(B, T, Hq, Hkv, 0, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
   if ((ve == nullptr) != (ve_gate == nullptr)) return NC_ERR_INVALID_ARG;
   if (ve != nullptr && (!aligned16(ve) || (reinterpret_cast<uintptr_t>(ve_gate) & 1u) != 0)) return NC_ERR_INVALID_ARG;
-  const size_t need = ve != nullptr ? nc_attn_fwd_ve_workspace_bytes(B, T, Hq, Hkv, D)
-                                    : nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
+  const size_t need = fp8 ? nc_attn_fwd_fp8_workspace_bytes(B, T, Hq, Hkv, D)
+                          : ve != nullptr ? nc_attn_fwd_ve_workspace_bytes(B, T, Hq, Hkv, D)
+                                          : nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return NC_ERR_WORKSPACE;
 
+  // qn, kn (bf16, or e4m3 codes), then the work-item counter
+  const size_t es = fp8 ? 1 : 2;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* qn = ws;
-  void* kn = ws + 2ull * static_cast<size_t>(B) * T * Hq * D;
-  unsigned* item_ctr = reinterpret_cast<unsigned*>(ws + 2ull * static_cast<size_t>(B) * T * (Hq + Hkv) * D);
+  void* kn = ws + es * static_cast<size_t>(B) * T * Hq * D;
+  unsigned* item_ctr = reinterpret_cast<unsigned*>(ws + es * static_cast<size_t>(B) * T * (Hq + Hkv) * D);
   // with a value embedding, the mixed values follow the counter (the fwd workspace size, a multiple of 256)
   void* vmix = ve != nullptr ? ws + nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D) : nullptr;
   const void* vsrc = ve != nullptr ? vmix : v;
@@ -318,15 +341,22 @@ static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out
   if (n_sm < 1) return NC_ERR_CUDA;
   if (!fwd_split(B, T, Hq, Hkv, n_sm, G, P, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
 
+  // Q and K boxes: one 64-element half of a row in bf16 (two loads per tile), the whole 128-byte row in e4m3
+  const uint32_t qk_box = fp8 ? 128 : 64;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map_4d(&mq, qn, 128, Hq, T, B, 64, G, P, 1) || !make_map_4d(&mk, kn, 128, Hkv, T, B, 64, 1, 128, 1) ||
+  if (!make_map_4d(&mq, qn, 128, Hq, T, B, qk_box, G, P, 1, fp8) ||
+      !make_map_4d(&mk, kn, 128, Hkv, T, B, qk_box, 1, 128, 1, fp8) ||
       !make_map_4d(&mv, vsrc, 128, Hkv, T, B, 64, 1, 128, 1) || !make_map_4d(&mo, out, 128, Hq, T, B, 64, G, P, 1))
     return NC_ERR_CUDA;
 
   if (k1_begin != nullptr && cudaEventRecord(k1_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
   // qn leaves the prologue multiplied by log2(e) / sqrt(D): the attention kernel's scores are then base-2 logits.
-  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), scale_log2_for_d128() * qk_gain, item_ctr,
-                       stream, v, ve, ve_gate, vmix);
+  if (fp8)
+    st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), fp8_q_scale(qk_gain), item_ctr, stream,
+                         nullptr, nullptr, nullptr, nullptr, true, kFp8KScale);
+  else
+    st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, rope_table(rope_base), scale_log2_for_d128() * qk_gain,
+                         item_ctr, stream, v, ve, ve_gate, vmix);
   if (st != NC_OK) return st;
   if (k2_begin != nullptr && cudaEventRecord(k2_begin, stream) != cudaSuccess) return NC_ERR_CUDA;
 
@@ -346,9 +376,40 @@ static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out
   prm.Tk = T;
   prm.window = window;
   prm.wait_limit_ns = kWaitLimitNs;
-  st = launch_attention(mq, mk, mv, mv, mo, prm, n_sm, stream);
+  st = launch_attention(mq, mk, mv, mv, mo, prm, n_sm, stream, fp8);
   if (st == NC_OK && k2_end != nullptr && cudaEventRecord(k2_end, stream) != cudaSuccess) return NC_ERR_CUDA;
   return st;
+}
+
+size_t nc_attn_fwd_fp8_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
+  if (check_fwd_shapes(B, T, Hq, Hkv, D) != NC_OK) return 0;
+  return static_cast<size_t>(B) * T * (Hq + Hkv) * D + 256;
+}
+
+nc_status nc_attn_fwd_fp8_events(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,
+                                 int Hkv, int D, int window, float rope_base, float qk_gain, void* workspace,
+                                 size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin,
+                                 cudaEvent_t k2_end, cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace, workspace_bytes, k1_begin,
+                  k2_begin, k2_end, stream, nullptr, nullptr, true);
+}
+
+nc_status nc_attn_fwd_fp8(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv,
+                          int D, int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace, workspace_bytes, nullptr,
+                  nullptr, nullptr, stream, nullptr, nullptr, true);
+}
+
+nc_status nc_attn_qk_prologue_fp8(const void* q, const void* k, void* qn8, void* kn8, int B, int T, int Hq, int Hkv,
+                                  int D, float rope_base, float qk_gain, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || qn8 == nullptr || kn8 == nullptr) return NC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(qn8) || !aligned16(kn8)) return NC_ERR_INVALID_ARG;
+  if (!rope_base_ok(rope_base) || !(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
+  const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
+  if (st != NC_OK) return st;
+  return launch_prologue(q, k, qn8, kn8, B, T, Hq, Hkv, rope_table(rope_base), fp8_q_scale(qk_gain), nullptr, stream,
+                         nullptr, nullptr, nullptr, nullptr, true, kFp8KScale);
 }
 
 nc_status nc_attn_fwd_ws_events(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq,

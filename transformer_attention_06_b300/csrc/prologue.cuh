@@ -8,7 +8,8 @@
 // 8-lane group per token; lane kq of the group owns pairs [8kq, 8kq+8), i.e. two 16-byte slices of every head
 // vector of the token, so the cos/sin of the token are computed once and reused across all Hq + Hkv heads.  The
 // sum of squares is reduced across the group with three xor-shuffles.  The normalised q vectors may be multiplied
-// by a constant on the way out (the attention kernel takes the softmax scale log2(e) / sqrt(D) this way).
+// by a constant on the way out (the attention kernel takes the softmax scale log2(e) / sqrt(D) this way).  The fp8
+// variant writes qn and kn as e4m3 (1 byte per element) times per-tensor scales, for the e4m3 score contraction.
 #pragma once
 
 #include "common.cuh"
@@ -48,13 +49,18 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&y)[8]) {
                     pack_bf16x2(y[6], y[7]));
 }
 
+__device__ __forceinline__ uint2 pack8_e4m3(const float (&y)[8]) {
+  return make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7]));
+}
+
 // Processes `H` consecutive head vectors of one token (src/dst point at head 0), four at a time so that eight
-// 16-byte loads per lane are in flight before any arithmetic.
-__device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+// 16-byte loads per lane are in flight before any arithmetic.  OutT = __nv_bfloat16 writes bf16 rows of 256 bytes;
+// OutT = uint8_t writes e4m3 rows of 128 bytes (the values times `scale`, rounded to nearest even).
+template <typename OutT>
+__device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict__ src, OutT* __restrict__ dst,
                                                 int H, int kq, const float (&c)[8], const float (&s)[8],
                                                 unsigned gmask, float scale) {
   const uint4* in = reinterpret_cast<const uint4*>(src);
-  uint4* out = reinterpret_cast<uint4*>(dst);
   for (int h0 = 0; h0 < H; h0 += 4) {
     uint4 lo[4], hi[4];
 #pragma unroll
@@ -69,8 +75,15 @@ __device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict_
       if (h0 + u < H) {
         float y1[8], y2[8];
         rope_norm_slices(lo[u], hi[u], c, s, gmask, scale, y1, y2);
-        out[(h0 + u) * 16 + kq] = pack8_bf16(y1);
-        out[(h0 + u) * 16 + 8 + kq] = pack8_bf16(y2);
+        if constexpr (sizeof(OutT) == 1) {
+          uint2* out = reinterpret_cast<uint2*>(dst);
+          out[(h0 + u) * 16 + kq] = pack8_e4m3(y1);
+          out[(h0 + u) * 16 + 8 + kq] = pack8_e4m3(y2);
+        } else {
+          uint4* out = reinterpret_cast<uint4*>(dst);
+          out[(h0 + u) * 16 + kq] = pack8_bf16(y1);
+          out[(h0 + u) * 16 + 8 + kq] = pack8_bf16(y2);
+        }
       }
     }
   }
@@ -103,10 +116,12 @@ __device__ __forceinline__ void mix_values(const __nv_bfloat16* __restrict__ v, 
 constexpr int kPrologueThreads = 256;
 constexpr int kPrologueTokensPerBlock = kPrologueThreads / 8;
 
+// OutT: __nv_bfloat16 (qn, kn in bf16) or uint8_t (qn, kn in e4m3, scaled by q_scale and k_scale).
+template <typename OutT>
 __global__ void __launch_bounds__(kPrologueThreads)
     qk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                       __nv_bfloat16* __restrict__ qn, __nv_bfloat16* __restrict__ kn, int BT, int T, int Hq,
-                       int Hkv, const __grid_constant__ RopeTable tab, float q_scale, unsigned* zero_word,
+                       OutT* __restrict__ qn, OutT* __restrict__ kn, int BT, int T, int Hq,
+                       int Hkv, const __grid_constant__ RopeTable tab, float q_scale, float k_scale, unsigned* zero_word,
                        const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ ve,
                        const __nv_bfloat16* __restrict__ ve_gate, __nv_bfloat16* __restrict__ vmix) {
   // The attention kernel that follows in stream order may be scheduled now; it waits for this grid to complete
@@ -125,7 +140,7 @@ __global__ void __launch_bounds__(kPrologueThreads)
   rope_norm_heads(q + static_cast<size_t>(tok) * Hq * 128, qn + static_cast<size_t>(tok) * Hq * 128, Hq, kq, c, s,
                   gmask, q_scale);
   rope_norm_heads(k + static_cast<size_t>(tok) * Hkv * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq, c,
-                  s, gmask, 1.0f);
+                  s, gmask, k_scale);
   if (ve != nullptr)
     mix_values(v + static_cast<size_t>(tok) * Hkv * 128, ve + static_cast<size_t>(tok) * Hkv * 128,
                ve_gate + static_cast<size_t>(tok) * Hkv, vmix + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq);

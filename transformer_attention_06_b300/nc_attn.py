@@ -57,6 +57,10 @@ def _load():
         "nc_attn_decode_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp]),
         "nc_attn_decode": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
         "nc_attn_decode_noalloc": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]),
+        "nc_attn_fwd_fp8_workspace_bytes": (sz, [i, i, i, i, i]),
+        "nc_attn_fwd_fp8": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
+        "nc_attn_fwd_fp8_events": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp, vp, vp, vp]),
+        "nc_attn_qk_prologue_fp8": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, vp]),
         "nc_attn_status_string": (ctypes.c_char_p, [i]),
         "nc_attn_get_device_status": (i, [vp, i]),
         "nc_attn_selftest_wait_timeout": (i, [i, vp]),
@@ -193,6 +197,53 @@ def nc_attn_fwd(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, workspace=Non
                                    float(rope_base), _ptr(workspace), wsb, ev[0], ev[1], ev[2], _stream(stream))
     _check(st, "nc_attn_fwd")
     return out
+
+
+def nc_attn_fwd_fp8_workspace_bytes(B, T, Hq, Hkv, D=128):
+    return int(lib.nc_attn_fwd_fp8_workspace_bytes(B, T, Hq, Hkv, D))
+
+
+def nc_attn_fwd_fp8(q, k, v, out=None, window=-1, rope_base=ROPE_BASE, qk_gain=1.0, workspace=None, stream=None,
+                    events=None):
+    """Prefill forward with the score contraction on e4m3 operands (``nc_attn_fwd_fp8``): q [B,T,Hq,D], k and v
+    [B,T,Hkv,D] (bf16, CUDA, contiguous) -> out [B,T,Hq,D] bf16.  ``events``: optional (k1_begin, k2_begin, k2_end)
+    torch.cuda.Event objects recorded around the prologue and the attention kernel."""
+    _need(q, "q", 4)
+    _need(k, "k", 4)
+    _need(v, "v", 4)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, T, Hkv, D) or tuple(v.shape) != (B, T, Hkv, D):
+        raise ValueError(f"k/v shapes {tuple(k.shape)}/{tuple(v.shape)} do not match q {tuple(q.shape)}")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", 4)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have the shape of q")
+    if workspace is None:
+        workspace = _workspace("fwd", nc_attn_fwd_fp8_workspace_bytes(B, T, Hq, Hkv, D), q.device, zero=False)
+    wsb = workspace.numel() * workspace.element_size()
+    ev = [_event_handle(e, stream) for e in (events or (None, None, None))]
+    st = lib.nc_attn_fwd_fp8_events(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T, Hq, Hkv, D, int(window),
+                                    float(rope_base), float(qk_gain), _ptr(workspace), wsb, ev[0], ev[1], ev[2],
+                                    _stream(stream))
+    _check(st, "nc_attn_fwd_fp8")
+    return out
+
+
+def nc_attn_qk_prologue_fp8(q, k, qk_gain=1.0, rope_base=ROPE_BASE, stream=None):
+    """The e4m3 prologue alone: returns (qn8, kn8), uint8 tensors of q's and k's shapes holding the e4m3 codes of
+    norm(rope(q)) * s_q and norm(rope(k)) * s_k (``nc_attn_qk_prologue_fp8``)."""
+    _need(q, "q", 4)
+    _need(k, "k", 4)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    qn8 = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    kn8 = torch.empty(k.shape, dtype=torch.uint8, device=k.device)
+    st = lib.nc_attn_qk_prologue_fp8(_ptr(q), _ptr(k), _ptr(qn8), _ptr(kn8), B, T, Hq, Hkv, D, float(rope_base),
+                                     float(qk_gain), _stream(stream))
+    _check(st, "nc_attn_qk_prologue_fp8")
+    return qn8, kn8
 
 
 def nc_attn_bwd(q, k, v, dout, window=-1, rope_base=ROPE_BASE, qk_gain=1.0, workspace=None, stream=None):
