@@ -299,6 +299,8 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+ALL_SECTIONS = "e2e,prefill,fp8,decode,chunk,backward,cpu"
+
 LONG_WORKLOAD = (f"{LONG.name}: B={LONG.B} T={LONG.T} Hq={LONG.Hq} Hkv={LONG.Hkv} D={LONG.D}, one step = calls with "
                  f"windows {list(LONG.windows)} (sliding window and full causal), distinct seeded q,k,v per call")
 
@@ -408,6 +410,8 @@ def run_ours(args, ws, rank, local):
             d["attn_frac"] = d["attn_tflops"] / peaks["bf16_tflops"]
         return sec
 
+    sections = set(args.sections.split(","))
+
     # ---- headline: the long-context step, with clocks sampled during its timed region
     w = LONG
     clocks = ClockSampler(local)
@@ -429,7 +433,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- end to end through the public API with host buffers
     e2e = None
-    if not args.skip_e2e:
+    if "e2e" in sections:
         host = [(q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory(), torch.empty_like(o, device="cpu").pin_memory())
                 for (q, k, v, o, W) in layers]
         h2d = sum(x.numel() * x.element_size() for (q, k, v, _) in host for x in (q, k, v))
@@ -458,7 +462,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- the other prefill workloads, one section each (the long-context section is the headline's)
     prefill = {LONG.name: head}
-    if not args.skip_sections:
+    if "prefill" in sections:
         for wl in (TINY, DEPTH12, GQA):
             sec, _, lay, wsp_ = prefill_section(nc, wl, dev, flush, 20)
             prefill[wl.name] = add_fracs(sec)
@@ -468,7 +472,7 @@ def run_ours(args, ws, rank, local):
     # ---- the prefill with e4m3 score operands: half of the in-band FLOPs (Q K^T) on the 8-bit tensor path at twice the
     # bf16 rate, the other half (P V) in bf16, so its peak is 4/3 of the bf16 peak
     prefill_fp8 = None
-    if not args.skip_sections:
+    if "fp8" in sections:
         prefill_fp8 = {}
         peak8 = peaks["bf16_tflops"] * 4.0 / 3.0
         for wl in (LONG, GQA, DEPTH12):
@@ -486,7 +490,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- decode
     dec = None
-    if not args.skip_decode:
+    if "decode" in sections:
         dec = {}
         dw = DECODE
         for with_new in (False, True):
@@ -535,7 +539,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- chunked prefill against a KV cache
     chk = None
-    if not args.skip_decode:
+    if "chunk" in sections:
         cw = CHUNK
         d = chunk_inputs(cw.B, cw.Tq, cw.Hq, cw.Hkv, cw.D, cw.Tcap, seed=0)
         kc, vc = d["kcache"].to(dev), d["vcache"].to(dev)
@@ -577,7 +581,7 @@ def run_ours(args, ws, rank, local):
 
     # ---- backward pass (CUDA-core kernels) on the depth-12 layer shapes
     bwd = None
-    if not args.skip_decode:
+    if "backward" in sections:
         w = DEPTH12
         bq, bk, bv, bdo = (t.to(dev) for t in bwd_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, seed=0))
         bws = torch.empty(int(nc.lib.nc_attn_bwd_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D)), dtype=torch.uint8,
@@ -586,7 +590,7 @@ def run_ours(args, ws, rank, local):
         for W in sorted(set(w.windows)):
             nc.nc_attn_bwd(bq, bk, bv, bdo, window=W, workspace=bws)
             torch.cuda.synchronize()
-            n_b = 3
+            n_b = 10
             evs = [(mk(), mk()) for _ in range(n_b)]
             for i in range(n_b):
                 flush.fill_(i)
@@ -595,19 +599,21 @@ def run_ours(args, ws, rank, local):
                 evs[i][1].record(stream)
             torch.cuda.synchronize()
             us = dist_max(sum(a.elapsed_time(b) for a, b in evs) * 1e3 / n_b, ws)
-            fl = 2.5 * fwd_flops(w.B, w.T, w.Hq, w.D, W)
+            fl = 3.5 * fwd_flops(w.B, w.T, w.Hq, w.D, W)
             per_w[str(W)] = {"us_per_call": us, "tflops": fl / (us * 1e-6) / 1e12}
             tot_f += fl
             tot_us += us
         val = tot_f / (tot_us * 1e-6) / 1e12
         bwd = {"value": val, "unit": "TFLOP/s", "frac": val / peaks["bf16_tflops"], "windows": per_w,
-               "config": (f"{w.name} layer shapes, windows {sorted(set(w.windows))}; dq, dk, dv in fp32 from CUDA-core "
-                          f"kernels; FLOPs counted as 2.5x the forward's in-band FLOPs; L2 flushed before each call")}
+               "config": (f"{w.name} layer shapes, windows {sorted(set(w.windows))}; one nc_attn_bwd_ws call: the forward "
+                          f"recomputed for its row statistics, then dK/dV and dQ on tcgen05 and the norm/RoPE backward; "
+                          f"dq, dk, dv in fp32; FLOPs counted as 3.5x the forward's in-band FLOPs (2 products of the "
+                          f"forward, 5 of the backward); L2 flushed before each call")}
         del bq, bk, bv, bdo, bws
 
     st = nc.nc_attn_get_device_status(clear=True)
     cpu = None
-    if rank == 0 and not args.skip_cpu:
+    if rank == 0 and "cpu" in sections:
         cpu = cpu_baseline()
 
     if rank == 0:
@@ -652,10 +658,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--skip-decode", action="store_true")
-    ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--skip-sections", action="store_true", help="time only the headline step (and decode etc.)")
+    ap.add_argument("--sections", default=ALL_SECTIONS,
+                    help="comma-separated sections timed after the headline step (default: all of " + ALL_SECTIONS + ")")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     if args.impl == "reference":

@@ -162,8 +162,11 @@ def test_bwd_rejects_bad_arguments(nc):
     assert call(D=64) == U
     assert call() == WS
     need = nc.lib.nc_attn_bwd_workspace_bytes(1, 64, 4, 2, 128)
-    assert need >= 4 * 64 * 6 * 128
+    # qn, kn in bf16, then the row statistics: two fp32 values per row of each padded 128-row Q tile (G = 2: P = 64
+    # positions per tile, one tile per kv head)
+    assert need >= 2 * 64 * 6 * 128 + 2 * 2 * 128 * 4
     assert call(ws=P, wsb=need - 1) == WS
+    assert call(Hq=256, Hkv=1) == U             # group larger than one 128-row tile
 
 
 def test_fwd_ve_rejects_bad_arguments(nc):

@@ -1,243 +1,598 @@
-// K5: backward pass of the attention block on the CUDA cores (fp32), correctness first.
+// K5: backward pass of the attention block on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // What it computes: the gradients of sum(dout * out) with respect to the raw q, k and v of the prefill forward
 // (out = attention(norm(rope(q)), norm(rope(k)), v), causal with the window, logits scaled by qk_gain / sqrt(D),
 // contiguous GQA groups; "nanochat Admin & Developer Guide", section 3 -- the model trains through this block).
 // The chain rule, per (b, query head h, kv head g = h / G), with P = softmax(S), O = P V, c = qk_gain / sqrt(D):
 //   dV_g += P^T dO,  dP = dO V_g^T,  dS = P * (dP - rowsum(dO * O)),  dqn_h = c dS kn_g,  dkn_g += c dS^T qn_h;
-// then the RMSNorm backward dx = (dy - qn (dy . qn) / D) / r (r the forward's RMS, eps included) and the RoPE
+// then the RMSNorm backward dx = (dy - yn (dy . yn) / D) / r (r the forward's RMS, eps included) and the RoPE
 // backward, the rotation of each pair (i, i + D/2) by -t theta_i.
 //
-// Four kernels, one warp per output row, lane l holding dims [4 l', 4 l' + 4) of half l / 16 (l' = l % 16), so that
-// a RoPE pair (i, i + 64) sits in lanes l and l ^ 16; dot products over the 128 dims are xor-shuffle reductions.
-//   bwd_prep_kernel      qn, kn (fp32) and 1 / r of every q and k head vector;
-//   bwd_rowstats_kernel  per query row: log-sum-exp of its logits and rowsum(dO * O), with O recomputed by an online
-//                        softmax pass over the row's keys;
-//   bwd_dq_kernel        per query row: dqn over its keys, then the norm and RoPE backward -> dq;
-//   bwd_dkv_kernel       per key row of a kv head: dV and dkn over the queries (all heads of the group) that see it,
-//                        then the norm and RoPE backward -> dk.
-// No shared memory, no barriers, no waits.  The contractions run as warp dot products, far from the tensor cores'
-// rate: this kernel set establishes the gradients; a tcgen05 version is the next step for it.
+// The launches of one backward call (nc_attn_bwd_ws):
+//   1. the forward prologue (K1): qn' = qn c log2(e) and kn in bf16, exactly as the forward uses them;
+//   2. the forward attention kernel (K2) in its statistics mode: per query row the base-2 log-sum-exp of its logits
+//      and rowsum(dO * O) (O in fp32 before rounding), nothing else stored;
+//   3. bwd_kernel<false> (dK, dV): a work item is one 128-key tile of one (b, kv head); K and V stay in shared memory
+//      while the packed Q tiles (P = 128 / G positions x the G heads of the group, as in the forward) and dO tiles
+//      that see the keys stream through a 2-stage TMA ring.  Per Q tile:  S^T = K Q'^T and dP^T = V dO^T (tcgen05,
+//      fp32 in TMEM), P^T = 2^(S^T - lse) and dS^T = P^T (dP^T - rowsum) on the CUDA cores (bf16, back into TMEM over
+//      S^T and dP^T), then dV += P^T dO and dK += dS^T Q' (A from TMEM, B = the streamed tiles read MN-major);
+//   4. bwd_kernel<true> (dQ): a work item is one packed Q tile; Q' and dO stay, K and V tiles of its band stream.
+//      Per key tile: S = Q' K^T, dP = dO V^T, P and dS on the CUDA cores, dQ += dS K;
+//   5. bwd_norm_rope_kernel: the RMSNorm and RoPE backward of every dq and dk row, in place (memory-bound).
+// Step 4 recomputes S and dP (7 products per (key tile, Q tile) pair instead of 5) so that every gradient is written
+// by exactly one CTA: no atomics, and the result does not depend on the schedule.
+//
+// Scales: the products use qn' (base-2 logits, as in the forward), so dK = dS^T Q' carries a factor c log2(e): dkn =
+// ln 2 dK; dqn = c dQ with dQ = dS kn.  The probabilities and dS are rounded to bf16 for the tensor core, like P in
+// the forward; every accumulation is fp32.
 #pragma once
+
+#include <climits>
 
 #include "common.cuh"
 
 namespace nc {
 namespace bwd {
 
-constexpr int kWarpsPerBlock = 8;
+// ---- the RMSNorm + RoPE backward -----------------------------------------------------------------------------
+// The RMSNorm + RoPE backward of every q and k head vector, token-major like the forward prologue: an 8-lane group per
+// token, lane kq owning the pairs [8 kq, 8 kq + 8) (elements [8 kq, 8 kq + 8) and [64 + 8 kq, 64 + 8 kq + 8)) of every
+// head, so that a pair sits in one lane and the cos / sin of the token are computed once for its Hq + Hkv heads.  dq
+// and dk hold the gradients with respect to the normed vectors; each is replaced in place by the gradient with respect
+// to the raw vector: yn and r recomputed from the raw bf16 input in fp32, dx = (dy - yn (dy . yn) / D) / r, then the
+// rotation by -angle.  Sums over a head vector are reduced across the group with xor-shuffles.
+constexpr int kPostThreads = 256;
+constexpr int kPostTokensPerBlock = kPostThreads / 8;
+
+__device__ __forceinline__ void norm_rope_bwd_head(const __nv_bfloat16* __restrict__ x_raw, float* __restrict__ g,
+                                                   int kq, const float (&c)[8], const float (&s)[8], unsigned gmask) {
+  const uint4 lo = __ldg(reinterpret_cast<const uint4*>(x_raw) + kq);
+  const uint4 hi = __ldg(reinterpret_cast<const uint4*>(x_raw) + 8 + kq);
+  float4* gl = reinterpret_cast<float4*>(g + 8 * kq);
+  float4* gh = reinterpret_cast<float4*>(g + 64 + 8 * kq);
+  const float4 d0 = gl[0], d1 = gl[1], d2 = gh[0], d3 = gh[1];
+  const float dy1[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+  const float dy2[8] = {d2.x, d2.y, d2.z, d2.w, d3.x, d3.y, d3.z, d3.w};
+  const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+  float y1[8], y2[8];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x1 = (i & 1) ? bf16_hi(a[i >> 1]) : bf16_lo(a[i >> 1]);
+    const float x2 = (i & 1) ? bf16_hi(b[i >> 1]) : bf16_lo(b[i >> 1]);
+    y1[i] = fmaf(x1, c[i], x2 * s[i]);
+    y2[i] = fmaf(x2, c[i], -(x1 * s[i]));
+    ss = fmaf(y1[i], y1[i], fmaf(y2[i], y2[i], ss));
+  }
+  ss += __shfl_xor_sync(gmask, ss, 1);
+  ss += __shfl_xor_sync(gmask, ss, 2);
+  ss += __shfl_xor_sync(gmask, ss, 4);
+  const float inv_r = rsqrtf(ss * (1.0f / 128.0f) + kRmsEps);
+  float pr = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    y1[i] *= inv_r;
+    y2[i] *= inv_r;
+    pr = fmaf(dy1[i], y1[i], fmaf(dy2[i], y2[i], pr));
+  }
+  pr += __shfl_xor_sync(gmask, pr, 1);
+  pr += __shfl_xor_sync(gmask, pr, 2);
+  pr += __shfl_xor_sync(gmask, pr, 4);
+  pr *= 1.0f / 128.0f;
+  float o1[8], o2[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float e1 = (dy1[i] - y1[i] * pr) * inv_r, e2 = (dy2[i] - y2[i] * pr) * inv_r;
+    // transpose of the forward rotation (y1 = x1 c + x2 s, y2 = -x1 s + x2 c)
+    o1[i] = fmaf(e1, c[i], -(e2 * s[i]));
+    o2[i] = fmaf(e2, c[i], e1 * s[i]);
+  }
+  gl[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
+  gl[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
+  gh[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
+  gh[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
+}
+
+__global__ void __launch_bounds__(kPostThreads)
+    bwd_norm_rope_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, float* dq,
+                         float* dk, int BT, int T, int Hq, int Hkv, const __grid_constant__ RopeTable tab) {
+  const int tok = blockIdx.x * kPostTokensPerBlock + (threadIdx.x >> 3);
+  const int kq = threadIdx.x & 7;
+  if (tok >= BT) return;  // whole 8-lane groups leave together
+  const unsigned gmask = 0xFFu << ((threadIdx.x & 31) & ~7);
+  const float pos = static_cast<float>(tok % T);
+  float c[8], s[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rope_cos_sin(pos, tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
+  for (int h = 0; h < Hq; ++h)
+    norm_rope_bwd_head(q + (static_cast<size_t>(tok) * Hq + h) * 128, dq + (static_cast<size_t>(tok) * Hq + h) * 128,
+                       kq, c, s, gmask);
+  for (int h = 0; h < Hkv; ++h)
+    norm_rope_bwd_head(k + (static_cast<size_t>(tok) * Hkv + h) * 128,
+                       dk + (static_cast<size_t>(tok) * Hkv + h) * 128, kq, c, s, gmask);
+}
+
+// ---- tcgen05 kernels ---------------------------------------------------------------------------------------------
+constexpr int kThreads = 384;
+constexpr int kStages = 2;
+constexpr int kHalfBytes = 128 * 128;        // one 64-column half of a 128-row bf16 tile
+constexpr int kTileBytes = 2 * kHalfBytes;   // 32 KB
+constexpr int kEwWarps = 8;                  // warps 0-7: elementwise step and epilogue
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kRegsEw = 208, kRegsOther = 88;  // 2 x 128 x 208 + 128 x 88 = 384 x 168
+constexpr uint32_t kTmemCols = 512;
+// TMEM: X = S^T / P^T (dK,dV) or S (dQ); Y = dP^T / dS^T or dP / dS; accumulators dK, dV (dK,dV) or dQ.
+constexpr uint32_t kColX = 0, kColY = 128, kColAcc0 = 256, kColAcc1 = 384;
+constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // A, B both K-major (smem)
+constexpr uint32_t kIdescTM = idesc_bf16_f32(128, 128, false, true);   // A from TMEM, B MN-major (smem)
+
+// Shared memory: A1, A2 (resident per item), kStages x (B1, B2), kStages slots of the (lse, rowsum) vectors of the
+// streamed Q tiles (dK,dV kernel; 128 + 128 floats each), barriers, scheduler slots.
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + 2 * kTileBytes;
+constexpr int kOffVec = kOffB + kStages * 2 * kTileBytes;
+constexpr int kVecBytes = 2 * 128 * 4;
+constexpr int kOffBar = kOffVec + kStages * kVecBytes;
+constexpr int kBarAFull = 0;
+constexpr int kBarAEmpty = 1;
+constexpr int kBarBFull = 2;                          // [kStages]
+constexpr int kBarBEmpty = kBarBFull + kStages;       // [kStages]
+constexpr int kBarXFull = kBarBEmpty + kStages;
+constexpr int kBarYFull = kBarXFull + 1;
+constexpr int kBarPFull = kBarYFull + 1;
+constexpr int kBarDsFull = kBarPFull + 1;
+constexpr int kBarAccDone = kBarDsFull + 1;
+constexpr int kBarAccFree = kBarAccDone + 1;
+constexpr int kBarSchedFull = kBarAccFree + 1;        // [2]
+constexpr int kBarSchedEmpty = kBarSchedFull + 2;     // [2]
+constexpr int kBarMmaFinal = kBarSchedEmpty + 2;
+constexpr int kNumBars = kBarMmaFinal + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kAlignSlack = 768;
+constexpr int kSmemBytes = kOffMisc + 32 + kAlignSlack;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
-  const __nv_bfloat16* q;     // [B, T, Hq, 128]
-  const __nv_bfloat16* k;     // [B, T, Hkv, 128]
-  const __nv_bfloat16* v;     // [B, T, Hkv, 128]
-  const __nv_bfloat16* dout;  // [B, T, Hq, 128]
-  float* dq;                  // [B, T, Hq, 128]
-  float* dk;                  // [B, T, Hkv, 128]
-  float* dv;                  // [B, T, Hkv, 128]
-  float* qn;                  // [B, T, Hq, 128]  workspace
-  float* kn;                  // [B, T, Hkv, 128] workspace
-  float* inv_rq;              // [B, T, Hq]       workspace
-  float* inv_rk;              // [B, T, Hkv]      workspace
-  float* lse;                 // [B, T, Hq]       workspace
-  float* drow;                // [B, T, Hq]       workspace: rowsum(dO * O)
-  int B, T, Hq, Hkv, G, window;
-  float c;                    // qk_gain / sqrt(128)
+  float* dst_a;        // dK,dV kernel: dk rows (gradient w.r.t. kn); dQ kernel: dq rows (w.r.t. qn)
+  float* dst_b;        // dK,dV kernel: dv rows; dQ kernel: unused
+  const float* lse;    // [B, Hkv, n_qtiles, 128]: base-2 log-sum-exp of every packed query row
+  const float* drow;   // same layout: rowsum(dO * O)
+  unsigned* item_ctr;  // zero at launch
+  int B, T, Hq, Hkv, G, P, n_qtiles, n_ktiles, n_items;
+  int window;          // -1: unbounded (the host maps windows >= T to -1)
+  float scale_a;       // factor on the dst_a accumulator: ln 2 (dK) or qk_gain / sqrt(128) (dQ)
+  unsigned long long wait_limit_ns;
 };
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
+struct Item {
+  int b, g;
+  int tile;    // key tile (dK,dV) or Q tile (dQ) of the item
+  int lo, hi;  // streamed tiles: Q tiles (dK,dV) or key tiles (dQ)
+};
 
-// Dims of lane l: half l / 16, indices [4 (l % 16), 4 (l % 16) + 4) within the half.
-__device__ __forceinline__ int lane_dim0(int lane) { return (lane >> 4) * 64 + (lane & 15) * 4; }
-
-__device__ __forceinline__ void load4_bf16(const __nv_bfloat16* p, float (&x)[4]) {
-  const uint2 u = *reinterpret_cast<const uint2*>(p);
-  x[0] = bf16_lo(u.x);
-  x[1] = bf16_hi(u.x);
-  x[2] = bf16_lo(u.y);
-  x[3] = bf16_hi(u.y);
-}
-
-__device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
-  const float4 u = *reinterpret_cast<const float4*>(p);
-  x[0] = u.x;
-  x[1] = u.y;
-  x[2] = u.z;
-  x[3] = u.w;
-}
-
-__device__ __forceinline__ void store4(float* p, const float (&x)[4]) {
-  *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
-}
-
-__device__ __forceinline__ float dot4(const float (&a)[4], const float (&b)[4]) {
-  return fmaf(a[0], b[0], fmaf(a[1], b[1], fmaf(a[2], b[2], a[3] * b[3])));
-}
-
-// cos / sin of this lane's four pair angles at position t.
-__device__ __forceinline__ void lane_cos_sin(const RopeTable& tab, int lane, int t, float (&cs)[4], float (&sn)[4]) {
-  const int i0 = (lane & 15) * 4;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) rope_cos_sin(static_cast<float>(t), tab.hi[i0 + e], tab.lo[i0 + e], cs[e], sn[e]);
-}
-
-// Rotation of the pairs by +angle (forward RoPE, sign = 1) or -angle (its backward, sign = -1).
-__device__ __forceinline__ void rotate(float (&x)[4], const float (&cs)[4], const float (&sn)[4], int lane,
-                                       float sign) {
-  const bool first = lane < 16;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
-    const float s = sign * sn[e];
-    // forward: y_i = x_i c + x_{i+64} s,  y_{i+64} = -x_i s + x_{i+64} c
-    x[e] = first ? fmaf(x[e], cs[e], other * s) : fmaf(x[e], cs[e], -other * s);
+template <bool kDQ>
+__device__ __forceinline__ Item decode_item(const Params& p, int item) {
+  Item it;
+  const int bh = p.B * p.Hkv;
+  const int ord = item / bh;
+  const int bg = item - ord * bh;
+  it.b = bg / p.Hkv;
+  it.g = bg - it.b * p.Hkv;
+  if (!kDQ) {
+    // key tile ord: queries at positions [128 ord, min(T - 1, 128 ord + 127 + window)] see its keys; under a causal
+    // mask the first key tiles are seen by the most queries, so they come first
+    it.tile = ord;
+    const int k0 = ord * 128;
+    const int last = p.window < 0 ? p.T - 1 : min(p.T - 1, k0 + 127 + p.window);
+    it.lo = k0 / p.P;
+    it.hi = last / p.P;
+  } else {
+    // Q tile n_qtiles - 1 - ord (latest, heaviest first): keys [max(0, t0 - window), t_last]
+    it.tile = p.n_qtiles - 1 - ord;
+    const int t0 = it.tile * p.P;
+    const int t_last = min(t0 + p.P, p.T) - 1;
+    it.lo = (p.window < 0 ? 0 : max(0, t0 - p.window)) / 128;
+    it.hi = t_last / 128;
   }
+  return it;
 }
 
-// qn, kn and 1 / r for every q head vector (rows [0, B T Hq)) and k head vector (the next B T Hkv rows).
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) bwd_prep_kernel(const Params p, const __grid_constant__ RopeTable tab) {
-  const int lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  const long long nq = static_cast<long long>(p.B) * p.T * p.Hq, nk = static_cast<long long>(p.B) * p.T * p.Hkv;
-  if (row >= nq + nk) return;
-  const bool is_q = row < nq;
-  const long long r = is_q ? row : row - nq;
-  const int H = is_q ? p.Hq : p.Hkv;
-  const int t = static_cast<int>((r / H) % p.T);
-  const int d0 = lane_dim0(lane);
-  float x[4];
-  load4_bf16((is_q ? p.q : p.k) + r * 128 + d0, x);
-  float cs[4], sn[4];
-  lane_cos_sin(tab, lane, t, cs, sn);
-  rotate(x, cs, sn, lane, 1.f);
-  const float inv_r = rsqrtf(warp_sum(dot4(x, x)) * (1.f / 128.f) + kRmsEps);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) x[e] *= inv_r;
-  store4((is_q ? p.qn : p.kn) + r * 128 + d0, x);
-  if (lane == 0) (is_q ? p.inv_rq : p.inv_rk)[r] = inv_r;
+// 32-column visibility mask of the column interval [lo, hi] within columns [c0, c0 + 32).
+__device__ __forceinline__ uint32_t interval_mask(int lo, int hi, int c0) {
+  const int a = lo - c0, b = hi - c0;
+  const uint32_t m_hi = b >= 31 ? ~0u : (b < 0 ? 0u : (2u << b) - 1u);
+  const uint32_t m_lo = a <= 0 ? ~0u : (a > 31 ? 0u : ~((1u << a) - 1u));
+  return m_hi & m_lo;
 }
 
-// Per query row (b, t, h): lse = log sum_j exp(s_j) and drow = dO . O, O = softmax(s) V recomputed online.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) bwd_rowstats_kernel(const Params p) {
+// kDQ = false: dK and dV; kDQ = true: dQ.  Maps: tmQ = qn' and tmDO = dout ([B, T, Hq, 128], box {64, G, P, 1}),
+// tmK = kn and tmV = v ([B, T, Hkv, 128], box {64, 1, 128, 1}); all bf16, 128-byte swizzle.
+template <bool kDQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem + kOffA;
+  uint8_t* sB = smem + kOffB;
+  float* sVec = reinterpret_cast<float*>(smem + kOffVec);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* a_full = bars + kBarAFull;        // A1, A2 (and the dQ item's vectors) landed       TMA -> MMA, ew
+  uint64_t* a_empty = bars + kBarAEmpty;      // every product reading A1, A2 done                MMA -> TMA
+  uint64_t* b_full = bars + kBarBFull;        // [kStages] B1, B2 (and the dK,dV vectors) landed  TMA -> MMA, ew
+  uint64_t* b_empty = bars + kBarBEmpty;      // [kStages] every product reading the stage done   MMA -> TMA
+  uint64_t* x_full = bars + kBarXFull;        // X = A1 B1^T in TMEM                              MMA -> ew
+  uint64_t* y_full = bars + kBarYFull;        // Y = A2 B2^T in TMEM                              MMA -> ew
+  uint64_t* p_full = bars + kBarPFull;        // P^T written over X (dK,dV; one arrival per warp) ew -> MMA
+  uint64_t* ds_full = bars + kBarDsFull;      // dS written over Y (one arrival per warp)         ew -> MMA
+  uint64_t* acc_done = bars + kBarAccDone;    // the item's last accumulation complete            MMA -> ew
+  uint64_t* acc_free = bars + kBarAccFree;    // accumulators read by the epilogue (per warp)     ew -> MMA
+  uint64_t* sched_full = bars + kBarSchedFull;
+  uint64_t* sched_empty = bars + kBarSchedEmpty;
+  uint64_t* mma_final = bars + kBarMmaFinal;
+  int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = misc + 1;
+  int* sched = misc + 2;  // [2]
+
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (row >= static_cast<long long>(p.B) * p.T * p.Hq) return;
-  const int h = static_cast<int>(row % p.Hq);
-  const long long bt = row / p.Hq;
-  const int t = static_cast<int>(bt % p.T), b = static_cast<int>(bt / p.T), g = h / p.G;
-  const int d0 = lane_dim0(lane);
-  float qv[4];
-  load4(p.qn + row * 128 + d0, qv);
-  const int lo = p.window < 0 ? 0 : max(0, t - p.window);
-  float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int j = lo; j <= t; ++j) {
-    const long long kr = (static_cast<long long>(b) * p.T + j) * p.Hkv + g;
-    float kv[4], vv[4];
-    load4(p.kn + kr * 128 + d0, kv);
-    load4_bf16(p.v + kr * 128 + d0, vv);
-    const float s = p.c * warp_sum(dot4(qv, kv));
-    const float m2 = fmaxf(m, s);
-    const float a = expf(m - m2), e = expf(s - m2);
-    l = fmaf(l, a, e);
-#pragma unroll
-    for (int d = 0; d < 4; ++d) o[d] = fmaf(o[d], a, e * vv[d]);
-    m = m2;
+  const unsigned long long lim = p.wait_limit_ns;
+  if (static_cast<int>(smem - smem_raw) > kAlignSlack) {
+    if (threadIdx.x == 0) raise_status(NC_DEV_SMEM_BASE);
+    return;
   }
-  float dov[4];
-  load4_bf16(p.dout + row * 128 + d0, dov);
-  const float inv_l = 1.f / l;
-#pragma unroll
-  for (int d = 0; d < 4; ++d) o[d] *= inv_l;
-  const float dr = warp_sum(dot4(dov, o));
-  if (lane == 0) {
-    p.lse[row] = m + logf(l);
-    p.drow[row] = dr;
+  const int GP = p.G * p.P;  // rows of a packed Q tile that hold queries
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(b_full + s, 1);
+      mbar_init(b_empty + s, 1);
+    }
+    mbar_init(x_full, 1);
+    mbar_init(y_full, 1);
+    mbar_init(p_full, kEwWarps);
+    mbar_init(ds_full, kEwWarps);
+    mbar_init(acc_done, 1);
+    mbar_init(acc_free, kEwWarps);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sched_full + s, 1);
+      mbar_init(sched_empty + s, 2);
+    }
+    mbar_init(mma_final, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
   }
-}
-
-// Norm backward then RoPE backward of this lane's 4 dims of dy (gradient w.r.t. the normed vector yn).
-__device__ __forceinline__ void norm_rope_bwd(float (&dy)[4], const float (&yn)[4], float inv_r, const RopeTable& tab,
-                                              int lane, int t) {
-  const float proj = warp_sum(dot4(dy, yn)) * (1.f / 128.f);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) dy[e] = (dy[e] - yn[e] * proj) * inv_r;
-  float cs[4], sn[4];
-  lane_cos_sin(tab, lane, t, cs, sn);
-  rotate(dy, cs, sn, lane, -1.f);
-}
-
-// Per query row (b, t, h): dq.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) bwd_dq_kernel(const Params p, const __grid_constant__ RopeTable tab) {
-  const int lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (row >= static_cast<long long>(p.B) * p.T * p.Hq) return;
-  const int h = static_cast<int>(row % p.Hq);
-  const long long bt = row / p.Hq;
-  const int t = static_cast<int>(bt % p.T), b = static_cast<int>(bt / p.T), g = h / p.G;
-  const int d0 = lane_dim0(lane);
-  float qv[4], dov[4];
-  load4(p.qn + row * 128 + d0, qv);
-  load4_bf16(p.dout + row * 128 + d0, dov);
-  const float lse = p.lse[row], dr = p.drow[row];
-  const int lo = p.window < 0 ? 0 : max(0, t - p.window);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int j = lo; j <= t; ++j) {
-    const long long kr = (static_cast<long long>(b) * p.T + j) * p.Hkv + g;
-    float kv[4], vv[4];
-    load4(p.kn + kr * 128 + d0, kv);
-    load4_bf16(p.v + kr * 128 + d0, vv);
-    const float s = p.c * warp_sum(dot4(qv, kv));
-    const float dp = warp_sum(dot4(dov, vv));
-    const float ds = expf(s - lse) * (dp - dr);
-#pragma unroll
-    for (int d = 0; d < 4; ++d) acc[d] = fmaf(ds, kv[d], acc[d]);
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
   }
-#pragma unroll
-  for (int d = 0; d < 4; ++d) acc[d] *= p.c;
-  norm_rope_bwd(acc, qv, p.inv_rq[row], tab, lane, t);
-  store4(p.dq + row * 128 + d0, acc);
-}
-
-// Per key row (b, j, g): dk and dv over every query (of every head of the group) that sees key j.
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) bwd_dkv_kernel(const Params p, const __grid_constant__ RopeTable tab) {
-  const int lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (row >= static_cast<long long>(p.B) * p.T * p.Hkv) return;
-  const int g = static_cast<int>(row % p.Hkv);
-  const long long bj = row / p.Hkv;
-  const int j = static_cast<int>(bj % p.T), b = static_cast<int>(bj / p.T);
-  const int d0 = lane_dim0(lane);
-  float kv[4], vv[4];
-  load4(p.kn + row * 128 + d0, kv);
-  load4_bf16(p.v + row * 128 + d0, vv);
-  const int hi = p.window < 0 ? p.T - 1 : min(p.T - 1, j + p.window);
-  float dk_acc[4] = {0.f, 0.f, 0.f, 0.f}, dv_acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int t = j; t <= hi; ++t) {
-    for (int jh = 0; jh < p.G; ++jh) {
-      const long long qr = (static_cast<long long>(b) * p.T + t) * p.Hq + g * p.G + jh;
-      float qv[4], dov[4];
-      load4(p.qn + qr * 128 + d0, qv);
-      load4_bf16(p.dout + qr * 128 + d0, dov);
-      const float s = p.c * warp_sum(dot4(qv, kv));
-      const float dp = warp_sum(dot4(dov, vv));
-      const float pr = expf(s - p.lse[qr]);
-      const float ds = pr * (dp - p.drow[qr]);
-#pragma unroll
-      for (int d = 0; d < 4; ++d) {
-        dv_acc[d] = fmaf(pr, dov[d], dv_acc[d]);
-        dk_acc[d] = fmaf(ds, qv[d], dk_acc[d]);
+  if (GP < 128 && threadIdx.x < 256) {
+    // Rows of the packed Q / dO tiles that TMA never fills (128 is not a multiple of G) are zeroed once, so that a
+    // zero probability never meets a non-finite value in a product.  dQ: the resident A tiles; dK,dV: every stage.
+    const int r = threadIdx.x & 127;
+    if (r >= GP) {
+      const int nbuf = kDQ ? 2 : 2 * kStages;
+      for (int bi = (threadIdx.x >> 7); bi < nbuf; bi += 2) {
+        uint8_t* base = (kDQ ? sA : sB) + bi * kTileBytes;
+        uint4* r0 = reinterpret_cast<uint4*>(base + r * 128);
+        uint4* r1 = reinterpret_cast<uint4*>(base + kHalfBytes + r * 128);
+        for (int i = 0; i < 8; ++i) {
+          r0[i] = make_uint4(0, 0, 0, 0);
+          r1[i] = make_uint4(0, 0, 0, 0);
+        }
       }
     }
   }
-  store4(p.dv + row * 128 + d0, dv_acc);
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t q_bytes = 2u * 128u * static_cast<uint32_t>(GP);  // one packed Q or dO tile: box {64, G, P, 1} x 2
+
+  if (warp >= kEwWarps) {
+    warpgroup_reg_dec<kRegsOther>();
+    if (warp == kProducerWarp && lane == 0) {
+      // ---------------------------------------------------------------- scheduler + TMA producer
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmDO);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int nb = 0;   // B stages filled so far
+      int na = 0;   // A fills so far
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (k >= 2 && !(ok = mbar_wait(sched_empty + slot, ((k >> 1) - 1) & 1, lim, abort_flag))) break;
+        const int item = static_cast<int>(atomicAdd(p.item_ctr, 1u));
+        sched[slot] = item < p.n_items ? item : -1;
+        mbar_arrive(sched_full + slot);
+        if (item >= p.n_items) break;
+        const Item it = decode_item<kDQ>(p, item);
+        // A tiles once every product of the previous item that reads them has completed
+        if (na > 0 && !(ok = mbar_wait(a_empty, (na - 1) & 1, lim, abort_flag))) break;
+        if (!kDQ) {
+          mbar_arrive_expect_tx(a_full, 2 * kTileBytes);
+          tma_load_4d(sA, &tmK, a_full, 0, it.g, it.tile * 128, it.b);
+          tma_load_4d(sA + kHalfBytes, &tmK, a_full, 64, it.g, it.tile * 128, it.b);
+          tma_load_4d(sA + kTileBytes, &tmV, a_full, 0, it.g, it.tile * 128, it.b);
+          tma_load_4d(sA + kTileBytes + kHalfBytes, &tmV, a_full, 64, it.g, it.tile * 128, it.b);
+        } else {
+          const int t0 = it.tile * p.P;
+          mbar_arrive_expect_tx(a_full, 2 * q_bytes);
+          tma_load_4d(sA, &tmQ, a_full, 0, it.g * p.G, t0, it.b);
+          tma_load_4d(sA + kHalfBytes, &tmQ, a_full, 64, it.g * p.G, t0, it.b);
+          tma_load_4d(sA + kTileBytes, &tmDO, a_full, 0, it.g * p.G, t0, it.b);
+          tma_load_4d(sA + kTileBytes + kHalfBytes, &tmDO, a_full, 64, it.g * p.G, t0, it.b);
+        }
+        ++na;
+        for (int j = it.lo; ok && j <= it.hi; ++j, ++nb) {
+          const int st = nb % kStages;
+          if (nb >= kStages && !(ok = mbar_wait(b_empty + st, ((nb / kStages) - 1) & 1, lim, abort_flag))) break;
+          uint8_t* b1 = sB + (2 * st) * kTileBytes;
+          uint8_t* b2 = b1 + kTileBytes;
+          if (!kDQ) {
+            const int t0 = j * p.P;
+            const size_t vi = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.n_qtiles + j) * 128;
+            mbar_arrive_expect_tx(b_full + st, 2 * q_bytes + kVecBytes);
+            tma_load_4d(b1, &tmQ, b_full + st, 0, it.g * p.G, t0, it.b);
+            tma_load_4d(b1 + kHalfBytes, &tmQ, b_full + st, 64, it.g * p.G, t0, it.b);
+            tma_load_4d(b2, &tmDO, b_full + st, 0, it.g * p.G, t0, it.b);
+            tma_load_4d(b2 + kHalfBytes, &tmDO, b_full + st, 64, it.g * p.G, t0, it.b);
+            bulk_load(sVec + st * 256, p.lse + vi, 512, b_full + st);
+            bulk_load(sVec + st * 256 + 128, p.drow + vi, 512, b_full + st);
+          } else {
+            mbar_arrive_expect_tx(b_full + st, 2 * kTileBytes);
+            tma_load_4d(b1, &tmK, b_full + st, 0, it.g, j * 128, it.b);
+            tma_load_4d(b1 + kHalfBytes, &tmK, b_full + st, 64, it.g, j * 128, it.b);
+            tma_load_4d(b2, &tmV, b_full + st, 0, it.g, j * 128, it.b);
+            tma_load_4d(b2 + kHalfBytes, &tmV, b_full + st, 64, it.g, j * 128, it.b);
+          }
+        }
+      }
+      // every copy this CTA started lands before the CTA exits (already true on the normal path)
+      for (int t = max(0, nb - kStages); t < nb; ++t) mbar_wait(b_full + t % kStages, (t / kStages) & 1, lim, nullptr);
+      if (na > 0) mbar_wait(a_full, (na - 1) & 1, lim, nullptr);
+    } else if (warp == kMmaWarp) {
+      // ---------------------------------------------------------------- MMA issuer (lane 0; the warp waits together)
+      const bool leader = lane == 0;
+      const uint32_t aA = smem_u32(sA), aB = smem_u32(sB);
+      constexpr uint64_t kTileDesc = kTileBytes >> 4;
+      const uint64_t dA = sdesc_sw128(aA, 16, 1024);            // K-major: A1 at +0, A2 at +1 tile
+      const uint64_t dBk = sdesc_sw128(aB, 16, 1024);           // K-major view of the B tiles
+      const uint64_t dBm = sdesc_sw128(aB, kHalfBytes, 1024);   // MN-major view of the B tiles
+      const uint32_t tX = tbase + kColX, tY = tbase + kColY, tAcc0 = tbase + kColAcc0, tAcc1 = tbase + kColAcc1;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, lim, abort_flag));
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (leader) umma_commit(bar);
+        __syncwarp();
+      };
+      // D (tmem) = A (smem tile ai) B (smem tile bi)^T, both K-major
+      auto mma_kk = [&](uint32_t d, int ai, int bi) {
+        if (leader) {
 #pragma unroll
-  for (int d = 0; d < 4; ++d) dk_acc[d] *= p.c;
-  norm_rope_bwd(dk_acc, kv, p.inv_rk[row], tab, lane, j);
-  store4(p.dk + row * 128 + d0, dk_acc);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+            umma_ss(d, dA + ai * kTileDesc + off, dBk + bi * kTileDesc + off, kIdescKK, kk > 0 ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+      };
+      // D (tmem) (+)= A (bf16 pairs in tmem, half h's columns at [64 h, 64 h + 32)) B (smem tile bi, MN-major)
+      auto mma_tm = [&](uint32_t d, uint32_t a, int bi, uint32_t acc0) {
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(d, a + (kk >> 2) * 64 + (kk & 3) * 8,
+                    dBm + bi * kTileDesc + static_cast<uint64_t>((kk * 2048) >> 4), kIdescTM, kk > 0 ? 1u : acc0);
+        }
+        __syncwarp();
+      };
+      int nb = 0, ns = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!(ok = wait(sched_full + slot, (k >> 1) & 1))) break;
+        const int item = sched[slot];
+        __syncwarp();
+        if (leader) mbar_arrive(sched_empty + slot);
+        if (item < 0) break;
+        const Item it = decode_item<kDQ>(p, item);
+        if (!(ok = wait(a_full, k & 1))) break;
+        for (int j = it.lo; j <= it.hi; ++j, ++nb, ++ns) {
+          const int st = nb % kStages;
+          const int b1 = 2 * st, b2 = 2 * st + 1;
+          if (!(ok = wait(b_full + st, (nb / kStages) & 1))) break;
+          tc_fence_after_sync();
+          mma_kk(tX, 0, b1);  // dK,dV: S^T = K Q'^T     dQ: S = Q' K^T
+          commit(x_full);
+          mma_kk(tY, 1, b2);  // dK,dV: dP^T = V dO^T   dQ: dP = dO V^T
+          commit(y_full);
+          if (j == it.hi) commit(a_empty);
+          // the accumulators of the previous item must have been read out before the first accumulation
+          if (j == it.lo && k > 0 && !(ok = wait(acc_free, (k - 1) & 1))) break;
+          const uint32_t acc0 = j > it.lo ? 1u : 0u;
+          if (!kDQ) {
+            if (!(ok = wait(p_full, ns & 1))) break;
+            tc_fence_after_sync();
+            mma_tm(tAcc1, tX, b2, acc0);  // dV += P^T dO
+            if (!(ok = wait(ds_full, ns & 1))) break;
+            tc_fence_after_sync();
+            mma_tm(tAcc0, tY, b1, acc0);  // dK += dS^T Q'
+          } else {
+            if (!(ok = wait(ds_full, ns & 1))) break;
+            tc_fence_after_sync();
+            mma_tm(tAcc0, tY, b1, acc0);  // dQ += dS K
+          }
+          commit(b_empty + st);
+          if (j == it.hi) commit(acc_done);
+        }
+      }
+      if (leader) umma_commit(mma_final);  // every issued product completes before TMEM is released
+      __syncwarp();
+      mbar_wait(mma_final, 0, lim, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------------ elementwise + epilogue (warps 0-7)
+    warpgroup_reg_inc<kRegsEw>();
+    const int r = threadIdx.x & 127;   // TMEM lane = row of X, Y and the accumulators
+    const int h = warp >> 2;           // column half [64 h, 64 h + 64)
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tX = tbase + lane_base + kColX, tY = tbase + lane_base + kColY;
+    constexpr uint32_t kBarAll = 1;    // named barrier of the 256 elementwise threads
+    int nb = 0, ns = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(sched_full + slot, (k >> 1) & 1, lim, abort_flag));
+      if (!named_bar_and(kBarAll, 2 * 128, ok)) break;
+      const int item = sched[slot];
+      named_bar_sync(kBarAll, 2 * 128);
+      if (threadIdx.x == 0) mbar_arrive(sched_empty + slot);
+      if (item < 0) break;
+      const Item it = decode_item<kDQ>(p, item);
+      bool fail = false;
+      // dQ: this row's query position, log-sum-exp and rowsum, read from global memory (written by an earlier
+      // launch); the padding rows of a tile hold zeros there, and see no key below
+      int t_row = 0;
+      float lse_r = 0.f, dr_r = 0.f;
+      if (kDQ) {
+        t_row = it.tile * p.P + r / p.G;
+        const size_t vi = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.n_qtiles + it.tile) * 128 + r;
+        lse_r = __ldg(p.lse + vi);
+        dr_r = __ldg(p.drow + vi);
+      }
+      const bool row_ok = !kDQ || (r < GP && t_row < p.T);
+      const int key_row = it.tile * 128 + r;  // dK,dV: this row's key position
+      for (int j = it.lo; !fail && j <= it.hi; ++j, ++nb, ++ns) {
+        const int st = nb % kStages;
+        // visible columns of this thread's row: one interval [lo_c, hi_c] of the tile's 128 columns
+        int lo_c, hi_c;
+        if (!kDQ) {
+          // columns = packed query rows of Q tile j: c -> position j P + c / G
+          const int t0 = j * p.P;
+          lo_c = p.G * (key_row - t0);
+          hi_c = min(GP, p.G * (p.T - t0)) - 1;
+          if (p.window >= 0) hi_c = min(hi_c, p.G * (key_row + p.window - t0) + p.G - 1);
+        } else {
+          // columns = keys j 128 + c
+          hi_c = row_ok ? t_row - j * 128 : -1;
+          lo_c = p.window < 0 ? INT_MIN / 2 : hi_c - p.window;
+        }
+        const float* vec = sVec + st * 256;  // dK,dV: lse and rowsum of the columns (Q tile j), landed with B
+        if (!kDQ) {
+          fail = !__all_sync(0xffffffffu, mbar_wait(b_full + st, (nb / kStages) & 1, lim, abort_flag));
+          if (fail) break;
+        }
+        fail = !__all_sync(0xffffffffu, mbar_wait(x_full, ns & 1, lim, abort_flag));
+        if (fail) break;
+        tc_fence_after_sync();
+        // ---- probabilities: P = 2^(X - lse) on the visible columns, 0 elsewhere
+        float pv[2][32];
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c0 = 64 * h + 32 * c2;
+          uint32_t sv[32];
+          tmem_ld32(tX + c0, sv);
+          tmem_ld_wait(sv);
+          const uint32_t vis = interval_mask(lo_c, hi_c, c0);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float l = kDQ ? lse_r : vec[c0 + c];
+            pv[c2][c] = ((vis >> c) & 1u) ? ex2_approx(__uint_as_float(sv[c]) - l) : 0.f;
+          }
+          if (!kDQ) {  // P^T is an operand of dV += P^T dO: bf16 pairs over the S^T columns just read
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[c2][2 * c], pv[c2][2 * c + 1]);
+            tmem_st16(tX + 64 * h + 16 * c2, pk);
+          }
+        }
+        if (!kDQ) {
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full);
+        }
+        // ---- dS = P (dP - rowsum), bf16 pairs over the dP columns just read
+        fail = !__all_sync(0xffffffffu, mbar_wait(y_full, ns & 1, lim, abort_flag));
+        if (fail) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c0 = 64 * h + 32 * c2;
+          uint32_t dv[32];
+          tmem_ld32(tY + c0, dv);
+          tmem_ld_wait(dv);
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float d0 = kDQ ? dr_r : vec[128 + c0 + 2 * c];
+            const float d1 = kDQ ? dr_r : vec[128 + c0 + 2 * c + 1];
+            pk[c] = pack_bf16x2(pv[c2][2 * c] * (__uint_as_float(dv[2 * c]) - d0),
+                                pv[c2][2 * c + 1] * (__uint_as_float(dv[2 * c + 1]) - d1));
+          }
+          tmem_st16(tY + 64 * h + 16 * c2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full);
+      }
+      if (!named_bar_and(kBarAll, 2 * 128, !fail)) break;
+      // ---- epilogue: the accumulators, scaled, to global memory (fp32)
+      fail = !__all_sync(0xffffffffu, mbar_wait(acc_done, k & 1, lim, abort_flag));
+      if (!named_bar_and(kBarAll, 2 * 128, !fail)) break;
+      tc_fence_after_sync();
+      size_t row_off = 0;
+      bool store = false;
+      if (!kDQ) {
+        store = key_row < p.T;
+        row_off = ((static_cast<size_t>(it.b) * p.T + key_row) * p.Hkv + it.g) * 128;
+      } else {
+        const int t = it.tile * p.P + r / p.G;
+        store = r < GP && t < p.T;
+        row_off = ((static_cast<size_t>(it.b) * p.T + t) * p.Hq + it.g * p.G + r % p.G) * 128;
+      }
+#pragma unroll
+      for (int a = 0; a < (kDQ ? 1 : 2); ++a) {
+        float* dst = (a == 0 ? p.dst_a : p.dst_b) + row_off + 64 * h;
+        const float sc = a == 0 ? p.scale_a : 1.f;
+        const uint32_t tacc = tbase + lane_base + (a == 0 ? kColAcc0 : kColAcc1) + 64 * h;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t av[32];
+          tmem_ld32(tacc + 32 * c2, av);
+          tmem_ld_wait(av);
+          if (store) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              reinterpret_cast<float4*>(dst + 32 * c2)[w] =
+                  make_float4(__uint_as_float(av[4 * w]) * sc, __uint_as_float(av[4 * w + 1]) * sc,
+                              __uint_as_float(av[4 * w + 2]) * sc, __uint_as_float(av[4 * w + 3]) * sc);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_free);
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, kTmemCols);
+  }
 }
 
 }  // namespace bwd

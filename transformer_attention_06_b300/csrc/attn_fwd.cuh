@@ -31,8 +31,8 @@
 //               and a commit only tracks its own thread's MMAs), so the tensor core serves whichever tile is ready
 //               while the other tile's softmax runs.  K, V stages and the Q tiles are released by one commit from
 //               each issuer (barriers of count 2).
-// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512); P_X overlays the first 64
-// columns of S_X.  Shared memory: Q_A, Q_B 32 KB each, 2-stage K and V rings of 32 KB tiles, all in the
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512); P_X (bf16 pairs) overlays S_X:
+// the P of keys [64 h, 64 h + 64) goes to columns [64 h, 64 h + 32), inside the S columns the same thread read.  Shared memory: Q_A, Q_B 32 KB each, 2-stage K and V rings of 32 KB tiles, all in the
 // 128-byte-swizzled K-major layout written by TMA, and one 32 KB output staging tile in the same layout.
 #pragma once
 
@@ -118,6 +118,15 @@ struct Params {
   int tiles_per_item;                 // 2 (Q tiles A and B share every K/V tile), or 1 when pairs would leave SMs idle
   int Tk;                             // key rows per sequence that the K / V maps address (T, or the cache size)
   unsigned long long wait_limit_ns;
+  // Row statistics for the backward pass (all null in a plain forward).  When `lse` is set, every query row's
+  // log2(sum_j 2^S_j) of its base-2 logits is written at lse[((b Hkv + g) n_qtiles + m) 128 + r] (Q tile m, tile row
+  // r); when `drow` is also set, rowsum(dout * out) of the row (fp32 out, before rounding) goes to the same index of
+  // drow, dout being [B, T, Hq, 128] bf16.  `store_out` = 0 skips writing out.
+  float* lse;
+  float* drow;
+  const __nv_bfloat16* dout;
+  int n_qtiles;
+  int store_out;
 };
 
 // Key-tile range of one Q tile: tiles [lo, hi] intersect its band; n = 0 when the tile lies past T.  Query rows
@@ -411,9 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int st, uint32_t acc0) {  // O_X (+)= P_X V (V from stage st)
         if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tO, tS + kk * 8, dv0 + st * kTileDesc + static_cast<uint64_t>((kk * 2048) >> 4), kIdescPV,
-                    kk > 0 ? 1u : acc0);
+          for (int kk = 0; kk < 8; ++kk)  // P of keys [16 kk, 16 kk + 16): columns 64 (kk / 4) + 8 (kk % 4)
+            umma_ts(tO, tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                    dv0 + st * kTileDesc + static_cast<uint64_t>((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
           umma_commit(o_done + x);
         }
         __syncwarp();
@@ -538,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // P = 2^S rounded to bf16, written over this half's part of the S row (keys [64 h, 64 h + 64) -> packed
-          // P columns [32 h, 32 h + 32)).  All 32 pairs are computed before the two TMEM stores (which the compiler
+          // P columns [64 h, 64 h + 32), which only this thread reads as S).  All 32 pairs are computed before the two TMEM stores (which the compiler
           // cannot move code across) so that the exponentials of the whole half row interleave.  The row sum adds
           // the bf16 values the P.V product uses, so that O / l weighs every key exactly as the product does (a row
           // with one visible key returns that key's value exactly).
@@ -554,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               rs[c & 3] = add_bf16x2_to_f32(pp, rs[c & 3]);
             }
           }
-          tmem_st16(tS + 32 * h, pk[0]);
-          tmem_st16(tS + 32 * h + 16, pk[1]);
+          tmem_st16(tS + 64 * h, pk[0]);
+          tmem_st16(tS + 64 * h + 16, pk[1]);
           l[x] += (rs[0] + rs[1]) + (rs[2] + rs[3]);
           tmem_st_wait();
           tc_fence_before_sync();
@@ -580,8 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the staging tile is free once the previous tile's TMA store has read it
         if (threadIdx.x == 0) bulk_wait_read_all();
         if (!named_bar_and(kBarAll, 2 * kSoftThreads, !fail)) { ok = false; break; }
-        const float inv_l = 1.f / (lx[r] + lx[128 + r]);
+        const float l_row = lx[r] + lx[128 + r];
+        const float inv_l = 1.f / l_row;
         tc_fence_after_sync();
+        // Backward-pass statistics: this row's query position and head, and its part of rowsum(dout * O).
+        const int t_row = q.t0 + r / p.G;
+        const bool stats_row = row_in_box && t_row < p.T;
+        const __nv_bfloat16* dorow =
+            p.drow != nullptr && stats_row
+                ? p.dout + ((static_cast<size_t>(it.b) * p.T + t_row) * p.Hq + it.g * p.G + r % p.G) * 128 + 64 * h
+                : nullptr;
+        float dpart = 0.f;
         // O / l in bf16 into the staging tile: this thread's 64 columns are one 128-byte row of half h, laid out
         // with the 128-byte swizzle of the output map (16-byte chunk c of row r at chunk position c ^ (r % 8)).
         uint8_t* srow = sO + h * kHalfBytes + r * 128;
@@ -590,7 +608,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ov[32];
           tmem_ld32(tO + 64 * h + 32 * c2, ov);
           tmem_ld_wait(ov);
-          if (row_in_box) {
+          if (dorow != nullptr) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(dorow + 32 * c2) + w);
+              const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                dpart = fmaf(__uint_as_float(ov[8 * w + 2 * e]) * inv_l, bf16_lo(dw[e]), dpart);
+                dpart = fmaf(__uint_as_float(ov[8 * w + 2 * e + 1]) * inv_l, bf16_hi(dw[e]), dpart);
+              }
+            }
+          }
+          if (row_in_box && p.store_out) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               uint32_t q4[4];
@@ -607,8 +637,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free + x);  // the MMA may start the next item's P.V into O_X
+        if (p.drow != nullptr) xch[256 + h * 128 + r] = dpart;
         named_bar_sync(kBarAll, 2 * kSoftThreads);  // staging tile written; the row-sum area is free again
-        if (threadIdx.x == 0 && it.valid) {  // rows past T fall outside the tensor and are not written
+        if (p.lse != nullptr && h == 0) {
+          // Every row of the tile is written, the rows that hold no query with zeros.  The next tile's epilogue
+          // writes the exchange area only after a barrier this thread has not reached yet.
+          const size_t ri = ((static_cast<size_t>(it.b) * p.Hkv + it.g) * p.n_qtiles + q.t0 / p.P) * 128 + r;
+          p.lse[ri] = stats_row ? log2f(l_row) : 0.f;
+          if (p.drow != nullptr) p.drow[ri] = stats_row ? xch[256 + r] + xch[384 + r] : 0.f;
+        }
+        if (threadIdx.x == 0 && it.valid && p.store_out) {  // rows past T fall outside the tensor and are not written
           tma_store_4d(&tmO, sO, 0, it.g * p.G, q.t0, it.b);
           tma_store_4d(&tmO, sO + kHalfBytes, 64, it.g * p.G, q.t0, it.b);
           bulk_commit_group();

@@ -281,6 +281,15 @@ bool fwd_split(int B, int T, int Hq, int Hkv, int n_sm, int& G, int& P, int& n_p
   return static_cast<long long>(B) * Hkv * n_pairs <= 0x7fffffffLL;
 }
 
+template <bool kDQ>
+nc_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const nc::bwd::Params& prm, int n_sm, cudaStream_t stream) {
+  set_smem_attr_once(nc::bwd::bwd_kernel<kDQ>, nc::bwd::kSmemBytes, kDQ ? 19 : 18);
+  const int grid = std::min(n_sm, prm.n_items);
+  nc::bwd::bwd_kernel<kDQ><<<grid, nc::bwd::kThreads, nc::bwd::kSmemBytes, stream>>>(mq, mdo, mk, mv, prm);
+  return launch_status();
+}
+
 }  // namespace
 
 // =================================================================================================================
@@ -376,6 +385,11 @@ static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out
   prm.Tk = T;
   prm.window = window;
   prm.wait_limit_ns = kWaitLimitNs;
+  prm.lse = nullptr;
+  prm.drow = nullptr;
+  prm.dout = nullptr;
+  prm.n_qtiles = (T + P - 1) / P;
+  prm.store_out = 1;
   st = launch_attention(mq, mk, mv, mv, mo, prm, n_sm, stream, fp8);
   if (st == NC_OK && k2_end != nullptr && cudaEventRecord(k2_end, stream) != cudaSuccess) return NC_ERR_CUDA;
   return st;
@@ -523,6 +537,11 @@ static nc_status chunk_impl(const void* q, const void* k_new, const void* v_new,
   prm.Tk = Tcap;
   prm.window = window;
   prm.wait_limit_ns = kWaitLimitNs;
+  prm.lse = nullptr;
+  prm.drow = nullptr;
+  prm.dout = nullptr;
+  prm.n_qtiles = (Tq + P - 1) / P;
+  prm.store_out = 1;
   return launch_attention(mq, mk, mv, mvt, mo, prm, n_sm, stream);
 }
 
@@ -554,28 +573,32 @@ nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_
                                   rope_base, ws, need, stream);
 }
 
-// Backward workspace: qn, kn (fp32), then 1/r of q and k rows, log-sum-exp and rowsum(dO * O) per query row, each
-// region 256-byte aligned.
+// Backward workspace: qn' and kn (bf16, as the forward writes them), three work-item counters (forward statistics,
+// dK/dV, dQ), then the per-row base-2 log-sum-exp and rowsum(dO * O) in the padded Q-tile layout
+// [B, Hkv, n_qtiles, 128]; each region 256-byte aligned.
 struct BwdLayout {
-  size_t qn, kn, inv_rq, inv_rk, lse, drow, total;
+  size_t qn, kn, ctr, lse, drow, total;
+  int G, P, n_qtiles;
 };
 
 static BwdLayout bwd_layout(int B, int T, int Hq, int Hkv) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t rq = static_cast<size_t>(B) * T * Hq, rk = static_cast<size_t>(B) * T * Hkv;
   BwdLayout L;
+  L.G = Hq / Hkv;
+  L.P = 128 / L.G;
+  L.n_qtiles = (T + L.P - 1) / L.P;
+  const size_t rows = static_cast<size_t>(B) * Hkv * L.n_qtiles * 128;
   L.qn = 0;
-  L.kn = up(L.qn + rq * 128 * 4);
-  L.inv_rq = up(L.kn + rk * 128 * 4);
-  L.inv_rk = up(L.inv_rq + rq * 4);
-  L.lse = up(L.inv_rk + rk * 4);
-  L.drow = up(L.lse + rq * 4);
-  L.total = up(L.drow + rq * 4);
+  L.kn = up(L.qn + static_cast<size_t>(B) * T * Hq * 128 * 2);
+  L.ctr = up(L.kn + static_cast<size_t>(B) * T * Hkv * 128 * 2);
+  L.lse = up(L.ctr + 16);
+  L.drow = up(L.lse + rows * 4);
+  L.total = up(L.drow + rows * 4);
   return L;
 }
 
 size_t nc_attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
-  if (check_fwd_shapes(B, T, Hq, Hkv, D) != NC_OK) return 0;
+  if (check_fwd_shapes(B, T, Hq, Hkv, D) != NC_OK || Hq / Hkv > 128) return 0;
   return bwd_layout(B, T, Hq, Hkv).total;
 }
 
@@ -590,42 +613,92 @@ nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void
     return NC_ERR_INVALID_ARG;
   if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
-  const nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
+  nc_status st = check_fwd_shapes(B, T, Hq, Hkv, D);
   if (st != NC_OK) return st;
-  const long long rows = static_cast<long long>(B) * T * (Hq + Hkv);
-  if (rows / nc::bwd::kWarpsPerBlock + 1 > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 128) return NC_ERR_UNSUPPORTED;
   const BwdLayout L = bwd_layout(B, T, Hq, Hkv);
+  if (static_cast<long long>(B) * Hkv * L.n_qtiles > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return NC_ERR_WORKSPACE;
+  const int n_sm = sm_count();
+  if (n_sm < 1) return NC_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  nc::bwd::Params p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
-  p.dout = static_cast<const __nv_bfloat16*>(dout);
-  p.dq = dq;
-  p.dk = dk;
-  p.dv = dv;
-  p.qn = reinterpret_cast<float*>(ws + L.qn);
-  p.kn = reinterpret_cast<float*>(ws + L.kn);
-  p.inv_rq = reinterpret_cast<float*>(ws + L.inv_rq);
-  p.inv_rk = reinterpret_cast<float*>(ws + L.inv_rk);
-  p.lse = reinterpret_cast<float*>(ws + L.lse);
-  p.drow = reinterpret_cast<float*>(ws + L.drow);
-  p.B = B;
-  p.T = T;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.G = Hq / Hkv;
-  p.window = window;
-  p.c = static_cast<float>(static_cast<double>(qk_gain) / std::sqrt(128.0));
+  void* qn = ws + L.qn;
+  void* kn = ws + L.kn;
+  unsigned* ctr = reinterpret_cast<unsigned*>(ws + L.ctr);
+  float* lse = reinterpret_cast<float*>(ws + L.lse);
+  float* drow = reinterpret_cast<float*>(ws + L.drow);
+  const int G = L.G, P = L.P;
+  const int w_eff = (window < 0 || window >= T - 1) ? -1 : window;  // windows >= T - 1 are plain causal
+
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map_4d(&mq, qn, 128, Hq, T, B, 64, G, P, 1) || !make_map_4d(&mk, kn, 128, Hkv, T, B, 64, 1, 128, 1) ||
+      !make_map_4d(&mv, v, 128, Hkv, T, B, 64, 1, 128, 1) || !make_map_4d(&mdo, dout, 128, Hq, T, B, 64, G, P, 1))
+    return NC_ERR_CUDA;
+  if (cudaMemsetAsync(ctr + 1, 0, 2 * sizeof(unsigned), stream) != cudaSuccess) return NC_ERR_CUDA;
+
+  // 1. qn' = qn log2(e) qk_gain / sqrt(D) and kn, as in the forward (zeroes the forward's work counter)
   const RopeTable tab = rope_table(rope_base);
-  constexpr int kThr = nc::bwd::kWarpsPerBlock * 32;
-  auto blocks = [](long long n) { return static_cast<unsigned>((n + nc::bwd::kWarpsPerBlock - 1) / nc::bwd::kWarpsPerBlock); };
-  const long long nq = static_cast<long long>(B) * T * Hq, nk = static_cast<long long>(B) * T * Hkv;
-  nc::bwd::bwd_prep_kernel<<<blocks(nq + nk), kThr, 0, stream>>>(p, tab);
-  nc::bwd::bwd_rowstats_kernel<<<blocks(nq), kThr, 0, stream>>>(p);
-  nc::bwd::bwd_dq_kernel<<<blocks(nq), kThr, 0, stream>>>(p, tab);
-  nc::bwd::bwd_dkv_kernel<<<blocks(nk), kThr, 0, stream>>>(p, tab);
+  st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, tab, scale_log2_for_d128() * qk_gain, ctr, stream);
+  if (st != NC_OK) return st;
+  // 2. the forward's row statistics (no output written: the output map points at qn', which has its shape)
+  int n_pairs = 0, tpi = 0, G2 = 0, P2 = 0;
+  if (!fwd_split(B, T, Hq, Hkv, n_sm, G2, P2, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
+  nc::fwd::Params fp;
+  fp.out = static_cast<__nv_bfloat16*>(qn);
+  fp.item_ctr = ctr;
+  fp.pos0 = nullptr;
+  fp.B = B;
+  fp.T = T;
+  fp.Hq = Hq;
+  fp.Hkv = Hkv;
+  fp.G = G;
+  fp.P = P;
+  fp.n_pairs = n_pairs;
+  fp.n_items = B * Hkv * n_pairs;
+  fp.window = window;
+  fp.tiles_per_item = tpi;
+  fp.Tk = T;
+  fp.wait_limit_ns = kWaitLimitNs;
+  fp.lse = lse;
+  fp.drow = drow;
+  fp.dout = static_cast<const __nv_bfloat16*>(dout);
+  fp.n_qtiles = L.n_qtiles;
+  fp.store_out = 0;
+  st = launch_attention(mq, mk, mv, mv, mq, fp, n_sm, stream);
+  if (st != NC_OK) return st;
+  // 3. dK (w.r.t. kn) and dV;  4. dQ (w.r.t. qn)
+  nc::bwd::Params bp;
+  bp.lse = lse;
+  bp.drow = drow;
+  bp.B = B;
+  bp.T = T;
+  bp.Hq = Hq;
+  bp.Hkv = Hkv;
+  bp.G = G;
+  bp.P = P;
+  bp.n_qtiles = L.n_qtiles;
+  bp.n_ktiles = (T + 127) / 128;
+  bp.window = w_eff;
+  bp.wait_limit_ns = kWaitLimitNs;
+  bp.dst_a = dk;
+  bp.dst_b = dv;
+  bp.item_ctr = ctr + 1;
+  bp.n_items = B * Hkv * bp.n_ktiles;
+  bp.scale_a = static_cast<float>(std::log(2.0));
+  st = launch_bwd<false>(mq, mdo, mk, mv, bp, n_sm, stream);
+  if (st != NC_OK) return st;
+  bp.dst_a = dq;
+  bp.dst_b = nullptr;
+  bp.item_ctr = ctr + 2;
+  bp.n_items = B * Hkv * L.n_qtiles;
+  bp.scale_a = static_cast<float>(static_cast<double>(qk_gain) / std::sqrt(128.0));
+  st = launch_bwd<true>(mq, mdo, mk, mv, bp, n_sm, stream);
+  if (st != NC_OK) return st;
+  // 5. the RMSNorm and RoPE backward of every q and k row, in place
+  const int BT = B * T;  // at most 2^31 - 33 (check_fwd_shapes)
+  const int blocks = (BT + nc::bwd::kPostTokensPerBlock - 1) / nc::bwd::kPostTokensPerBlock;
+  nc::bwd::bwd_norm_rope_kernel<<<blocks, nc::bwd::kPostThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), dq, dk, BT, T, Hq, Hkv, tab);
   return launch_status();
 }
 
