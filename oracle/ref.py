@@ -163,7 +163,7 @@ def attn_fwd_rows(q, k, v, window, rows, rope_base=ROPE_BASE, eps=RMS_EPS, qk_ga
 
 
 def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
-                rope_base=ROPE_BASE, eps=RMS_EPS, qk_gain=1.0):
+                rope_base=ROPE_BASE, eps=RMS_EPS, qk_gain=1.0, ve_new=None, ve_gate_new=None):
     """KV-cache single-token decode.
 
     q: [B, Hq, D] raw query of the new token; kcache, vcache: [B, Tcap, Hkv, D] (rows already roped+normed);
@@ -172,7 +172,8 @@ def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
     Returns (out [B, Hq, D] fp64, kn_new [B, Hkv, D] fp64 or None).  The query is roped at position p_b and
     normed.  Keys: cache rows 0..p_b-1 as given, plus, when k_new is given, norm(rope(k_new, p_b)) with v_new
     at position p_b.  Visible keys j satisfy p_b - j <= window (window >= 0).  An empty visible set (p_b = 0
-    and no new key) gives a zero row.
+    and no new key) gives a zero row.  With ve_new [B, Hkv, D] and ve_gate_new [B, Hkv], the new value is
+    ``value_mix(v_new, ve_new, ve_gate_new)`` (the gated value embedding of the new token).
     """
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
@@ -181,6 +182,8 @@ def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
     scale = qk_gain / np.sqrt(D)   # see QK_GAIN_NOTE
     out = np.zeros((B, Hq, D), dtype=np.float64)
     kn_new = None
+    if ve_new is not None:
+        v_new = value_mix(v_new, ve_new, ve_gate_new)
     if k_new is not None:
         kn_new = qk_prologue(np.asarray(k_new, dtype=np.float64)[:, None], np.asarray(cache_lens)[:, None],
                              rope_base, eps)[:, 0]
@@ -205,7 +208,7 @@ def attn_decode(q, kcache, vcache, cache_lens, window, k_new=None, v_new=None,
 
 
 def attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, window, rope_base=ROPE_BASE, eps=RMS_EPS,
-                       qk_gain=1.0):
+                       qk_gain=1.0, ve_new=None, ve_gate_new=None):
     """Chunked prefill against a KV cache -- Guide section 6 (the SDPA fallback's chunked / sliding-window
     inference case: the chunk's queries attend to the cache plus the chunk) and section 7 "KV cache" (in-place
     append at cache_seqlens).
@@ -217,12 +220,14 @@ def attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, window, rope
     position p_b + t.  The keys of sequence b are its cache rows 0..p_b-1 as given followed by
     norm(rope(k_new[b, t], p_b + t)), with the values vcache[b, :p_b] followed by v_new[b]; key position j is
     visible to query position i under ``visible``.  A p_b outside [0, Tcap - Tq] gives zero rows (and a zero
-    kn_new) for that sequence.
+    kn_new) for that sequence.  With ve_new [B, Tq, Hkv, D] and ve_gate_new [B, Tq, Hkv], the chunk's values are
+    ``value_mix(v_new, ve_new, ve_gate_new)`` (the gated value embedding of its tokens).
     """
     q = np.asarray(q, dtype=np.float64)
     B, Tq, Hq, D = q.shape
     Hkv = k_new.shape[2]
     Tcap = kcache.shape[1]
+    v_new = value_mix(v_new, ve_new, ve_gate_new)
     G = Hq // Hkv
     scale = qk_gain / np.sqrt(D)   # see QK_GAIN_NOTE
     out = np.zeros((B, Tq, Hq, D), dtype=np.float64)

@@ -81,3 +81,32 @@ def test_out_of_range_cache_length_gives_zero_rows():
     out, kn_new = ref.attn_prefill_chunk(q, kn, vn, kc, vc, [-1, 12, 13], -1)   # 12 + 8 = Tcap is the last valid
     assert np.all(out[0] == 0) and np.all(out[2] == 0) and np.all(kn_new[2] == 0)
     assert np.isfinite(out[1]).all() and np.abs(out[1]).max() > 0
+
+
+@pytest.mark.parametrize("W", [-1, 7])
+def test_value_embedding_chunk_and_decode_agree_with_the_prefill(W):
+    """The gated value embedding on the cache paths: a chunk against an empty cache is the prefill with the same
+    embedding, and a one-token chunk is a decode step whose new value carries it."""
+    B, T, Hq, Hkv = 2, 23, 4, 2
+    q, k, v = (f64(t) for t in fwd_inputs(B, T, Hq, Hkv, 128, seed=17))
+    rng = np.random.default_rng(5)
+    ve = rng.standard_normal((B, T, Hkv, 128))
+    gate = rng.standard_normal((B, T, Hkv)) * 2
+    kc = np.full((B, 40, Hkv, 128), np.nan)
+    out, _ = ref.attn_prefill_chunk(q, k, v, kc, kc, [0, 0], W, ve_new=ve, ve_gate_new=gate)
+    np.testing.assert_allclose(out, ref.attn_fwd(q, k, v, W, ve=ve, ve_gate=gate), rtol=0, atol=1e-12)
+    # one token at position p against a cache of the prefill's normed keys and mixed values
+    p = 11
+    pos = np.broadcast_to(np.arange(T), (B, T))
+    kn = ref.qk_prologue(k, pos)
+    vmix = ref.value_mix(v, ve, gate)
+    kc2 = np.zeros((B, 40, Hkv, 128))
+    vc2 = np.zeros((B, 40, Hkv, 128))
+    kc2[:, :p], vc2[:, :p] = kn[:, :p], vmix[:, :p]
+    full = ref.attn_fwd(q, k, v, W, ve=ve, ve_gate=gate)
+    one, _ = ref.attn_prefill_chunk(q[:, p:p + 1], k[:, p:p + 1], v[:, p:p + 1], kc2, vc2, [p, p], W,
+                                    ve_new=ve[:, p:p + 1], ve_gate_new=gate[:, p:p + 1])
+    dec, _ = ref.attn_decode(q[:, p], kc2, vc2, np.array([p, p]), W, k[:, p], v[:, p], ve_new=ve[:, p],
+                             ve_gate_new=gate[:, p])
+    np.testing.assert_allclose(one[:, 0], full[:, p], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dec, full[:, p], rtol=0, atol=1e-12)
