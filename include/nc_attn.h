@@ -178,7 +178,7 @@ nc_status nc_attn_decode_ex(const void* q, void* kcache, void* vcache, const int
                             int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream);
 
-/* ---- Gated value embedding (prefill) ---------------------------------------------------------------------------
+/* ---- Gated value embedding -------------------------------------------------------------------------------------
  * (The catalog pages list value embeddings with a sigmoid gate, in the ResFormer manner, among nanochat's
  * architectural additions.  The pages give no formula; the reading taken: v' = v + sigmoid(g) * ve, one gate logit g
  * per token and kv head.)  As nc_attn_fwd_ex with the attention run on v' instead of v:
@@ -192,6 +192,24 @@ size_t nc_attn_fwd_ve_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
 nc_status nc_attn_fwd_ve(const void* q, const void* k, const void* v, const void* ve, const void* ve_gate, void* out,
                          int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The same value embedding for the new tokens on the cache paths: the values appended to the cache (and attended
+ * to) are v_new' = v_new + sigmoid(ve_gate) * ve_new, formed in fp32 and rounded to bf16 once, as in nc_attn_fwd_ve.
+ *   nc_attn_prefill_chunk_ve: as nc_attn_prefill_chunk_ex, with ve_new:[B,Tq,Hkv,D] and ve_gate:[B,Tq,Hkv]
+ *     (the chunk's tokens); workspace as for nc_attn_prefill_chunk_ws.
+ *   nc_attn_decode_ve: as nc_attn_decode_ex with a new key and value (k_new, v_new required), with ve_new:[B,Hkv,D]
+ *     and ve_gate:[B,Hkv]; workspace as for nc_attn_decode_ws.
+ * ve tensors bf16 and 16-byte aligned, gates bf16 (2-byte aligned); both required (NC_ERR_INVALID_ARG otherwise).
+ */
+nc_status nc_attn_prefill_chunk_ve(const void* q, const void* k_new, const void* v_new, const void* ve_new,
+                                   const void* ve_gate, void* kcache, void* vcache, const int* cache_lens, void* out,
+                                   int B, int Tq, int Hq, int Hkv, int D, int Tcap, int window, float rope_base,
+                                   float qk_gain, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+nc_status nc_attn_decode_ve(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                            const void* k_new, const void* v_new, const void* ve_new, const void* ve_gate, int B,
+                            int Hq, int Hkv, int D, int Tcap, int window, float rope_base, float qk_gain,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---- Backward pass of the prefill forward -----------------------------------------------------------------------
  * ("nanochat Admin & Developer Guide", section 3: the model trains through this block.)  Gradients of

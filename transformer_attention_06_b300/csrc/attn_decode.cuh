@@ -93,6 +93,10 @@ struct Params {
   __nv_bfloat16* out;
   const __nv_bfloat16* k_new;
   const __nv_bfloat16* v_new;
+  // Gated value embedding of the new token (both null, or both set with k_new): the new value is
+  // v_new + sigmoid(ve_gate) ve_new, one gate logit per (b, kv head), rounded to bf16 once.
+  const __nv_bfloat16* ve_new;
+  const __nv_bfloat16* ve_gate;
   float* ws_ml;        // [C][2][G][2]   (m, l) of each partial, log2 domain
   float* ws_o;         // [C][2][G][128] unnormalised partial outputs
   unsigned* ws_cnt;    // [B][Hkv] arrival counters, zero between calls
@@ -100,6 +104,18 @@ struct Params {
   float scale_log2;    // log2(e) / sqrt(D)
   unsigned long long wait_limit_ns;
 };
+
+// Lane `lane`'s four elements [4 lane, 4 lane + 4) of the new value of (b, kv head g), as bf16 pairs: v_new, or with a
+// value embedding v_new + sigmoid(gate) ve_new in fp32, rounded to bf16.
+__device__ __forceinline__ uint2 new_value4(const Params& p, int b, int g, int lane) {
+  const size_t row = (static_cast<size_t>(b) * p.Hkv + g) * 128;
+  const uint2 vv = __ldg(reinterpret_cast<const uint2*>(p.v_new + row) + lane);
+  if (p.ve_new == nullptr) return vv;
+  const uint2 ee = __ldg(reinterpret_cast<const uint2*>(p.ve_new + row) + lane);
+  const float a = 1.f / (1.f + expf(-__bfloat162float(p.ve_gate[static_cast<size_t>(b) * p.Hkv + g])));
+  return make_uint2(pack_bf16x2(fmaf(a, bf16_lo(ee.x), bf16_lo(vv.x)), fmaf(a, bf16_hi(ee.x), bf16_hi(vv.x))),
+                    pack_bf16x2(fmaf(a, bf16_lo(ee.y), bf16_lo(vv.y)), fmaf(a, bf16_hi(ee.y), bf16_hi(vv.y))));
+}
 
 // ---- segment bookkeeping ------------------------------------------------------------------------------------------
 struct SeqInfo {
@@ -553,8 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           warp_rope_norm(p.k_new + (static_cast<size_t>(b) * p.Hkv + g) * 128, cs, sn, lane, y);
           reinterpret_cast<uint32_t*>(p.kcache + crow)[lane] = pack_bf16x2(y[0], y[1]);
           reinterpret_cast<uint32_t*>(p.kcache + crow + 64)[lane] = pack_bf16x2(y[2], y[3]);
-          const uint2 vv =
-              __ldg(reinterpret_cast<const uint2*>(p.v_new + (static_cast<size_t>(b) * p.Hkv + g) * 128) + lane);
+          const uint2 vv = new_value4(p, b, g, lane);
           reinterpret_cast<uint2*>(p.vcache + crow)[lane] = vv;
           for (int j = 0; j < G; ++j) outg[j * 32 + lane] = vv;
         } else {
@@ -844,8 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               new_k[64 + 2 * lane] = bf16_lo(w1);
               new_k[65 + 2 * lane] = bf16_hi(w1);
             } else if (ew == 1) {
-              const uint2 vv = __ldg(
-                  reinterpret_cast<const uint2*>(p.v_new + (static_cast<size_t>(b) * p.Hkv + g) * 128) + lane);
+              const uint2 vv = new_value4(p, b, g, lane);
               reinterpret_cast<uint2*>(p.vcache + crow)[lane] = vv;
               new_v[4 * lane] = bf16_lo(vv.x);
               new_v[4 * lane + 1] = bf16_hi(vv.x);

@@ -474,7 +474,7 @@ size_t nc_attn_prefill_chunk_workspace_bytes(int B, int Tq, int Hq, int Hkv, int
 static nc_status chunk_impl(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
                             const int* cache_lens, void* out, int B, int Tq, int Hq, int Hkv, int D, int Tcap,
                             int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const void* ve_new = nullptr, const void* ve_gate = nullptr) {
   if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   if (q == nullptr || k_new == nullptr || v_new == nullptr || kcache == nullptr || vcache == nullptr ||
       cache_lens == nullptr || out == nullptr)
@@ -484,6 +484,9 @@ static nc_status chunk_impl(const void* q, const void* k_new, const void* v_new,
     return NC_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return NC_ERR_INVALID_ARG;
   if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
+  if ((ve_new == nullptr) != (ve_gate == nullptr)) return NC_ERR_INVALID_ARG;
+  if (ve_new != nullptr && (!aligned16(ve_new) || (reinterpret_cast<uintptr_t>(ve_gate) & 1u) != 0))
+    return NC_ERR_INVALID_ARG;
   nc_status st = check_fwd_shapes(B, Tq, Hq, Hkv, D);
   if (st != NC_OK) return st;
   if (Tcap < Tq) return NC_ERR_INVALID_ARG;
@@ -517,7 +520,7 @@ static nc_status chunk_impl(const void* q, const void* k_new, const void* v_new,
       static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(qn), static_cast<__nv_bfloat16*>(kcache),
       static_cast<__nv_bfloat16*>(vcache), static_cast<__nv_bfloat16*>(vtail), static_cast<__nv_bfloat16*>(out),
       cache_lens, B, Tq, Hq, Hkv, Tcap, tok_blocks, rope_table(rope_base), scale_log2_for_d128() * qk_gain,
-      item_ctr);
+      item_ctr, static_cast<const __nv_bfloat16*>(ve_new), static_cast<const __nv_bfloat16*>(ve_gate));
   st = launch_status();
   if (st != NC_OK) return st;
 
@@ -559,6 +562,15 @@ nc_status nc_attn_prefill_chunk_ex(const void* q, const void* k_new, const void*
                                    size_t workspace_bytes, cudaStream_t stream) {
   return chunk_impl(q, k_new, v_new, kcache, vcache, cache_lens, out, B, Tq, Hq, Hkv, D, Tcap, window, rope_base,
                     qk_gain, workspace, workspace_bytes, stream);
+}
+
+nc_status nc_attn_prefill_chunk_ve(const void* q, const void* k_new, const void* v_new, const void* ve_new,
+                                   const void* ve_gate, void* kcache, void* vcache, const int* cache_lens, void* out,
+                                   int B, int Tq, int Hq, int Hkv, int D, int Tcap, int window, float rope_base,
+                                   float qk_gain, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (ve_new == nullptr || ve_gate == nullptr) return NC_ERR_INVALID_ARG;
+  return chunk_impl(q, k_new, v_new, kcache, vcache, cache_lens, out, B, Tq, Hq, Hkv, D, Tcap, window, rope_base,
+                    qk_gain, workspace, workspace_bytes, stream, ve_new, ve_gate);
 }
 
 nc_status nc_attn_prefill_chunk(const void* q, const void* k_new, const void* v_new, void* kcache, void* vcache,
@@ -711,11 +723,15 @@ size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, i
 static nc_status decode_impl(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
                              const void* k_new, const void* v_new, int B, int Hq, int Hkv, int D, int Tcap,
                              int window, float rope_base, float qk_gain, void* workspace, size_t workspace_bytes,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const void* ve_new = nullptr, const void* ve_gate = nullptr) {
   if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   const nc_status st =
       check_decode_args(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base);
   if (st != NC_OK) return st;
+  if ((ve_new == nullptr) != (ve_gate == nullptr)) return NC_ERR_INVALID_ARG;
+  if (ve_new != nullptr &&
+      (k_new == nullptr || !aligned16(ve_new) || (reinterpret_cast<uintptr_t>(ve_gate) & 1u) != 0))
+    return NC_ERR_INVALID_ARG;
   const DecodeLayout L = decode_layout(B, Hq, Hkv);
   if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return NC_ERR_WORKSPACE;
   const int grid = decode_grid();
@@ -735,6 +751,8 @@ static nc_status decode_impl(const void* q, void* kcache, void* vcache, const in
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
   prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  prm.ve_new = static_cast<const __nv_bfloat16*>(ve_new);
+  prm.ve_gate = static_cast<const __nv_bfloat16*>(ve_gate);
   prm.ws_cnt = reinterpret_cast<unsigned*>(ws + L.off_cnt);
   prm.ws_ml = reinterpret_cast<float*>(ws + L.off_ml);
   prm.ws_o = reinterpret_cast<float*>(ws + L.off_o);
@@ -783,6 +801,15 @@ nc_status nc_attn_decode_ex(const void* q, void* kcache, void* vcache, const int
                             cudaStream_t stream) {
   return decode_impl(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base,
                      qk_gain, workspace, workspace_bytes, stream);
+}
+
+nc_status nc_attn_decode_ve(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,
+                            const void* k_new, const void* v_new, const void* ve_new, const void* ve_gate, int B,
+                            int Hq, int Hkv, int D, int Tcap, int window, float rope_base, float qk_gain,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (ve_new == nullptr || ve_gate == nullptr || k_new == nullptr) return NC_ERR_INVALID_ARG;
+  return decode_impl(q, kcache, vcache, cache_lens, out, k_new, v_new, B, Hq, Hkv, D, Tcap, window, rope_base,
+                     qk_gain, workspace, workspace_bytes, stream, ve_new, ve_gate);
 }
 
 nc_status nc_attn_decode(const void* q, void* kcache, void* vcache, const int* cache_lens, void* out,

@@ -53,36 +53,62 @@ __device__ __forceinline__ uint2 pack8_e4m3(const float (&y)[8]) {
   return make_uint2(pack_e4m3x4(y[0], y[1], y[2], y[3]), pack_e4m3x4(y[4], y[5], y[6], y[7]));
 }
 
-// Processes `H` consecutive head vectors of one token (src/dst point at head 0), four at a time so that eight
-// 16-byte loads per lane are in flight before any arithmetic.  OutT = __nv_bfloat16 writes bf16 rows of 256 bytes;
-// OutT = uint8_t writes e4m3 rows of 128 bytes (the values times `scale`, rounded to nearest even).
+__device__ __forceinline__ void store_head(void* dst, int kq, const float (&y1)[8], const float (&y2)[8], bool e4m3) {
+  if (e4m3) {
+    uint2* out = reinterpret_cast<uint2*>(dst);
+    out[kq] = pack8_e4m3(y1);
+    out[8 + kq] = pack8_e4m3(y2);
+  } else {
+    uint4* out = reinterpret_cast<uint4*>(dst);
+    out[kq] = pack8_bf16(y1);
+    out[8 + kq] = pack8_bf16(y2);
+  }
+}
+
+// The Hq q heads then the Hkv k heads of one token (q, k, qn, kn point at the token's head 0), in rounds of four
+// heads whose loads are issued one round ahead: while a round is rotated, normalised and stored, the next round's
+// sixteen 16-byte loads per lane are in flight.  OutT = __nv_bfloat16 writes bf16 rows of 256 bytes; OutT = uint8_t
+// writes e4m3 rows of 128 bytes (the values times the scale, rounded to nearest even).
 template <typename OutT>
-__device__ __forceinline__ void rope_norm_heads(const __nv_bfloat16* __restrict__ src, OutT* __restrict__ dst,
-                                                int H, int kq, const float (&c)[8], const float (&s)[8],
-                                                unsigned gmask, float scale) {
-  const uint4* in = reinterpret_cast<const uint4*>(src);
-  for (int h0 = 0; h0 < H; h0 += 4) {
-    uint4 lo[4], hi[4];
+__device__ __forceinline__ void rope_norm_token(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                                                OutT* __restrict__ qn, OutT* __restrict__ kn, int Hq, int Hkv, int kq,
+                                                const float (&c)[8], const float (&s)[8], unsigned gmask,
+                                                float q_scale, float k_scale) {
+  constexpr bool kE4m3 = sizeof(OutT) == 1;
+  const int H = Hq + Hkv;
+  auto src = [&](int i) {
+    return reinterpret_cast<const uint4*>(i < Hq ? q + i * 128 : k + (i - Hq) * 128);
+  };
+  uint4 lo[2][4], hi[2][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (h0 + u < H) {
-        lo[u] = __ldg(in + (h0 + u) * 16 + kq);
-        hi[u] = __ldg(in + (h0 + u) * 16 + 8 + kq);
-      }
+  for (int u = 0; u < 4; ++u) {
+    if (u < H) {
+      lo[0][u] = __ldg(src(u) + kq);
+      hi[0][u] = __ldg(src(u) + 8 + kq);
     }
+  }
+  for (int h0 = 0; h0 < H; h0 += 8) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (h0 + u < H) {
-        float y1[8], y2[8];
-        rope_norm_slices(lo[u], hi[u], c, s, gmask, scale, y1, y2);
-        if constexpr (sizeof(OutT) == 1) {
-          uint2* out = reinterpret_cast<uint2*>(dst);
-          out[(h0 + u) * 16 + kq] = pack8_e4m3(y1);
-          out[(h0 + u) * 16 + 8 + kq] = pack8_e4m3(y2);
-        } else {
-          uint4* out = reinterpret_cast<uint4*>(dst);
-          out[(h0 + u) * 16 + kq] = pack8_bf16(y1);
-          out[(h0 + u) * 16 + 8 + kq] = pack8_bf16(y2);
+    for (int half = 0; half < 2; ++half) {
+      const int base = h0 + 4 * half;
+      if (base >= H) break;
+      const int nb = half ^ 1;  // buffer of the next round
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + 4 + u;
+        if (i < H) {
+          lo[nb][u] = __ldg(src(i) + kq);
+          hi[nb][u] = __ldg(src(i) + 8 + kq);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u;
+        if (i < H) {
+          float y1[8], y2[8];
+          rope_norm_slices(lo[half][u], hi[half][u], c, s, gmask, i < Hq ? q_scale : k_scale, y1, y2);
+          void* dst = i < Hq ? static_cast<void*>(qn + i * 128) : static_cast<void*>(kn + (i - Hq) * 128);
+          store_head(dst, kq, y1, y2, kE4m3);
         }
       }
     }
@@ -137,10 +163,9 @@ __global__ void __launch_bounds__(kPrologueThreads)
   float c[8], s[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) rope_cos_sin(pos, tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
-  rope_norm_heads(q + static_cast<size_t>(tok) * Hq * 128, qn + static_cast<size_t>(tok) * Hq * 128, Hq, kq, c, s,
-                  gmask, q_scale);
-  rope_norm_heads(k + static_cast<size_t>(tok) * Hkv * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq, c,
-                  s, gmask, k_scale);
+  rope_norm_token(q + static_cast<size_t>(tok) * Hq * 128, k + static_cast<size_t>(tok) * Hkv * 128,
+                  qn + static_cast<size_t>(tok) * Hq * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hq, Hkv, kq, c,
+                  s, gmask, q_scale, k_scale);
   if (ve != nullptr)
     mix_values(v + static_cast<size_t>(tok) * Hkv * 128, ve + static_cast<size_t>(tok) * Hkv * 128,
                ve_gate + static_cast<size_t>(tok) * Hkv, vmix + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq);
@@ -150,7 +175,7 @@ __global__ void __launch_bounds__(kPrologueThreads)
 // sliding-window inference"; section 7, the in-place KV-cache append).  For sequence b with p0 = cache_lens[b]:
 //   * the chunk's queries q[b, t] and keys k_new[b, t] are roped at position p0 + t and normed; qn goes to the
 //     workspace (times q_scale), the keys go straight into kcache[b, p0 + t] and the values v_new[b, t] into
-//     vcache[b, p0 + t];
+//     vcache[b, p0 + t] (with a value embedding: v_new + sigmoid(ve_gate) ve_new, rounded to bf16 once);
 //   * the V tile that holds the chunk's last key (rows [128 hb, 128 hb + 128), hb = (p0 + Tq - 1) / 128) is copied
 //     into vtail[b] with the rows past the chunk set to zero, so that the attention kernel never multiplies a zero
 //     probability by whatever the cache holds beyond its valid rows;
@@ -163,7 +188,8 @@ __global__ void __launch_bounds__(kPrologueThreads)
                           __nv_bfloat16* kcache, __nv_bfloat16* vcache, __nv_bfloat16* __restrict__ vtail,
                           __nv_bfloat16* __restrict__ out, const int* __restrict__ cache_lens, int B, int Tq, int Hq,
                           int Hkv, int Tcap, int n_tok_blocks, const __grid_constant__ RopeTable tab, float q_scale,
-                          unsigned* zero_word) {
+                          unsigned* zero_word, const __nv_bfloat16* __restrict__ ve_new,
+                          const __nv_bfloat16* __restrict__ ve_gate) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0u;
   const int grp = threadIdx.x >> 3;
@@ -186,10 +212,14 @@ __global__ void __launch_bounds__(kPrologueThreads)
 #pragma unroll
     for (int i = 0; i < 8; ++i) rope_cos_sin(static_cast<float>(pos), tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
     const size_t row = static_cast<size_t>(b) * Tcap + pos;  // cache row of this token
-    rope_norm_heads(q + static_cast<size_t>(tok) * Hq * 128, qn + static_cast<size_t>(tok) * Hq * 128, Hq, kq, c, s,
-                    gmask, q_scale);
-    rope_norm_heads(k_new + static_cast<size_t>(tok) * Hkv * 128, kcache + row * Hkv * 128, Hkv, kq, c, s, gmask,
-                    1.0f);
+    rope_norm_token(q + static_cast<size_t>(tok) * Hq * 128, k_new + static_cast<size_t>(tok) * Hkv * 128,
+                    qn + static_cast<size_t>(tok) * Hq * 128, kcache + row * Hkv * 128, Hq, Hkv, kq, c, s, gmask,
+                    q_scale, 1.0f);
+    if (ve_new != nullptr) {  // the chunk's values with their gated embedding, into the cache
+      mix_values(v_new + static_cast<size_t>(tok) * Hkv * 128, ve_new + static_cast<size_t>(tok) * Hkv * 128,
+                 ve_gate + static_cast<size_t>(tok) * Hkv, vcache + row * Hkv * 128, Hkv, kq);
+      return;
+    }
     const uint4* vs = reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(tok) * Hkv * 128);
     uint4* vd = reinterpret_cast<uint4*>(vcache + row * Hkv * 128);
     for (int i = kq; i < Hkv * 16; i += 8) vd[i] = __ldg(vs + i);
@@ -206,9 +236,15 @@ __global__ void __launch_bounds__(kPrologueThreads)
   if (key < p0) {  // an earlier cache row (not written by this kernel)
     const uint4* src = reinterpret_cast<const uint4*>(vcache + (static_cast<size_t>(b) * Tcap + key) * Hkv * 128);
     for (int e = kq; e < Hkv * 16; e += 8) d[e] = src[e];
-  } else if (key < p0 + Tq) {  // a row of the chunk
-    const uint4* src = reinterpret_cast<const uint4*>(v_new + (static_cast<size_t>(b) * Tq + (key - p0)) * Hkv * 128);
-    for (int e = kq; e < Hkv * 16; e += 8) d[e] = __ldg(src + e);
+  } else if (key < p0 + Tq) {  // a row of the chunk (mixed with its value embedding, as the cache row is)
+    const size_t tk = static_cast<size_t>(b) * Tq + (key - p0);
+    if (ve_new != nullptr) {
+      mix_values(v_new + tk * Hkv * 128, ve_new + tk * Hkv * 128, ve_gate + tk * Hkv,
+                 vtail + (static_cast<size_t>(b) * 128 + i) * Hkv * 128, Hkv, kq);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(v_new + tk * Hkv * 128);
+      for (int e = kq; e < Hkv * 16; e += 8) d[e] = __ldg(src + e);
+    }
   } else {
     for (int e = kq; e < Hkv * 16; e += 8) d[e] = zero4;
   }

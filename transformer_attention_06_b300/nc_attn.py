@@ -61,6 +61,8 @@ def _load():
         "nc_attn_fwd_fp8": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_fwd_fp8_events": (i, [vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp, vp, vp, vp]),
         "nc_attn_qk_prologue_fp8": (i, [vp, vp, vp, vp, i, i, i, i, i, f, f, vp]),
+        "nc_attn_prefill_chunk_ve": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, f, vp, sz, vp]),
+        "nc_attn_decode_ve": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_status_string": (ctypes.c_char_p, [i]),
         "nc_attn_get_device_status": (i, [vp, i]),
         "nc_attn_selftest_wait_timeout": (i, [i, vp]),
@@ -289,13 +291,14 @@ def nc_attn_qk_prologue(q, k, qn=None, kn=None, rope_base=ROPE_BASE, stream=None
 
 
 def nc_attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, out=None, window=-1, rope_base=ROPE_BASE,
-                          workspace=None, stream=None, qk_gain=1.0):
+                          workspace=None, stream=None, qk_gain=1.0, ve_new=None, ve_gate=None):
     """Chunked prefill against a KV cache.  q [B,Tq,Hq,D], k_new / v_new [B,Tq,Hkv,D] (raw), caches
     [B,Tcap,Hkv,D], cache_lens int32 [B] (device) -> out [B,Tq,Hq,D].
 
     The chunk's keys (roped at cache_lens[b] + t and normed) and values are written into the caches at rows
     cache_lens[b] .. cache_lens[b] + Tq - 1; query t attends to the cache rows up to its own position.  cache_lens is
-    not modified.
+    not modified.  ``ve_new`` [B,Tq,Hkv,D] and ``ve_gate`` [B,Tq,Hkv]: gated value embedding of the chunk's values
+    (``nc_attn_prefill_chunk_ve``).
     """
     _need(q, "q", 4)
     _need(k_new, "k_new", 4)
@@ -320,20 +323,33 @@ def nc_attn_prefill_chunk(q, k_new, v_new, kcache, vcache, cache_lens, out=None,
     nbytes = nc_attn_prefill_chunk_workspace_bytes(B, Tq, Hq, Hkv, D)
     if workspace is None:
         workspace = _workspace("chunk", nbytes, q.device, zero=False)
-    st = lib.nc_attn_prefill_chunk_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache), _ptr(cache_lens),
-                                      _ptr(out), B, Tq, Hq, Hkv, D, Tcap, int(window), float(rope_base),
-                                      float(qk_gain), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                      _stream(stream))
+    wsb = workspace.numel() * workspace.element_size()
+    if ve_new is not None or ve_gate is not None:
+        if ve_new is None or ve_gate is None:
+            raise ValueError("ve_new and ve_gate go together")
+        _need(ve_new, "ve_new", 4)
+        _need(ve_gate, "ve_gate", 3)
+        if tuple(ve_new.shape) != tuple(v_new.shape) or tuple(ve_gate.shape) != tuple(v_new.shape[:3]):
+            raise ValueError("ve_new must have v_new's shape and ve_gate [B, Tq, Hkv]")
+        st = lib.nc_attn_prefill_chunk_ve(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(ve_new), _ptr(ve_gate), _ptr(kcache),
+                                          _ptr(vcache), _ptr(cache_lens), _ptr(out), B, Tq, Hq, Hkv, D, Tcap,
+                                          int(window), float(rope_base), float(qk_gain), _ptr(workspace), wsb,
+                                          _stream(stream))
+    else:
+        st = lib.nc_attn_prefill_chunk_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kcache), _ptr(vcache),
+                                          _ptr(cache_lens), _ptr(out), B, Tq, Hq, Hkv, D, Tcap, int(window),
+                                          float(rope_base), float(qk_gain), _ptr(workspace), wsb, _stream(stream))
     _check(st, "nc_attn_prefill_chunk")
     return out
 
 
 def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=None, window=-1,
-                   rope_base=ROPE_BASE, workspace=None, stream=None, qk_gain=1.0):
+                   rope_base=ROPE_BASE, workspace=None, stream=None, qk_gain=1.0, ve_new=None, ve_gate=None):
     """Single-token decode.  q [B,Hq,D]; caches [B,Tcap,Hkv,D]; cache_lens int32 [B] (device) -> out [B,Hq,D].
 
     With k_new / v_new [B,Hkv,D], the new key (roped + normed at cache_lens[b]) and value are written into the caches
-    at row cache_lens[b] and attended to.  cache_lens is not modified.
+    at row cache_lens[b] and attended to.  cache_lens is not modified.  ``ve_new`` [B,Hkv,D] and ``ve_gate`` [B,Hkv]
+    (with k_new / v_new): gated value embedding of the new value (``nc_attn_decode_ve``).
     """
     _need(q, "q", 3)
     _need(kcache, "kcache", 4)
@@ -362,9 +378,21 @@ def nc_attn_decode(q, kcache, vcache, cache_lens, out=None, k_new=None, v_new=No
         if _ws_decode_tag.get(key, B * Hkv) != B * Hkv:
             workspace.zero_()
         _ws_decode_tag[key] = B * Hkv
-    st = lib.nc_attn_decode_ex(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
-                               _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base), float(qk_gain),
-                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    wsb = workspace.numel() * workspace.element_size()
+    if ve_new is not None or ve_gate is not None:
+        if ve_new is None or ve_gate is None or k_new is None:
+            raise ValueError("ve_new and ve_gate go together, with k_new / v_new")
+        _need(ve_new, "ve_new", 3)
+        _need(ve_gate, "ve_gate", 2)
+        if tuple(ve_new.shape) != (B, Hkv, D) or tuple(ve_gate.shape) != (B, Hkv):
+            raise ValueError("ve_new must be [B, Hkv, D] and ve_gate [B, Hkv]")
+        st = lib.nc_attn_decode_ve(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
+                                   _ptr(v_new), _ptr(ve_new), _ptr(ve_gate), B, Hq, Hkv, D, Tcap, int(window),
+                                   float(rope_base), float(qk_gain), _ptr(workspace), wsb, _stream(stream))
+    else:
+        st = lib.nc_attn_decode_ex(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_lens), _ptr(out), _ptr(k_new),
+                                   _ptr(v_new), B, Hq, Hkv, D, Tcap, int(window), float(rope_base), float(qk_gain),
+                                   _ptr(workspace), wsb, _stream(stream))
     _check(st, "nc_attn_decode")
     return out
 
