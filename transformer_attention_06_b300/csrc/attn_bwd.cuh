@@ -123,8 +123,15 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kRegsEw = 208, kRegsOther = 88;  // 2 x 128 x 208 + 128 x 88 = 384 x 168
 constexpr uint32_t kTmemCols = 512;
-// TMEM: X = S^T / P^T (dK,dV) or S (dQ); Y = dP^T / dS^T or dP / dS; accumulators dK, dV (dK,dV) or dQ.
+// TMEM: X = S^T / P^T (dK,dV) or S (dQ); Y = dP^T / dS^T or dP / dS; accumulators dK, dV (dK,dV), or dQ of the even
+// and of the odd items (dQ: the epilogue of one item overlaps the next item's first step).
 constexpr uint32_t kColX = 0, kColY = 128, kColAcc0 = 256, kColAcc1 = 384;
+
+// Accumulator buffer of the k-th item of a CTA and the phase of its barriers: the dQ kernel alternates two buffers.
+template <bool kDQ>
+__device__ __forceinline__ int acc_buf(int k) { return kDQ ? (k & 1) : 0; }
+template <bool kDQ>
+__device__ __forceinline__ uint32_t acc_phase(int k) { return kDQ ? ((k >> 1) & 1) : (k & 1); }
 constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // A, B both K-major (smem)
 constexpr uint32_t kIdescTM = idesc_bf16_f32(128, 128, false, true);   // A from TMEM, B MN-major (smem)
 
@@ -143,9 +150,9 @@ constexpr int kBarXFull = kBarBEmpty + kStages;
 constexpr int kBarYFull = kBarXFull + 1;
 constexpr int kBarPFull = kBarYFull + 1;
 constexpr int kBarDsFull = kBarPFull + 1;
-constexpr int kBarAccDone = kBarDsFull + 1;
-constexpr int kBarAccFree = kBarAccDone + 1;
-constexpr int kBarSchedFull = kBarAccFree + 1;        // [2]
+constexpr int kBarAccDone = kBarDsFull + 1;           // [2]: accumulator buffer
+constexpr int kBarAccFree = kBarAccDone + 2;          // [2]
+constexpr int kBarSchedFull = kBarAccFree + 2;        // [2]
 constexpr int kBarSchedEmpty = kBarSchedFull + 2;     // [2]
 constexpr int kBarMmaFinal = kBarSchedEmpty + 2;
 constexpr int kNumBars = kBarMmaFinal + 1;
@@ -227,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* y_full = bars + kBarYFull;        // Y = A2 B2^T in TMEM                              MMA -> ew
   uint64_t* p_full = bars + kBarPFull;        // P^T written over X (dK,dV; one arrival per warp) ew -> MMA
   uint64_t* ds_full = bars + kBarDsFull;      // dS written over Y (one arrival per warp)         ew -> MMA
-  uint64_t* acc_done = bars + kBarAccDone;    // the item's last accumulation complete            MMA -> ew
-  uint64_t* acc_free = bars + kBarAccFree;    // accumulators read by the epilogue (per warp)     ew -> MMA
+  uint64_t* acc_done = bars + kBarAccDone;    // [2] the item's last accumulation complete        MMA -> ew
+  uint64_t* acc_free = bars + kBarAccFree;    // [2] accumulators read by the epilogue (per warp) ew -> MMA
   uint64_t* sched_full = bars + kBarSchedFull;
   uint64_t* sched_empty = bars + kBarSchedEmpty;
   uint64_t* mma_final = bars + kBarMmaFinal;
@@ -256,8 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(y_full, 1);
     mbar_init(p_full, kEwWarps);
     mbar_init(ds_full, kEwWarps);
-    mbar_init(acc_done, 1);
-    mbar_init(acc_free, kEwWarps);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(acc_done + s, 1);
+      mbar_init(acc_free + s, kEwWarps);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sched_full + s, 1);
       mbar_init(sched_empty + s, 2);
@@ -415,8 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_kk(tY, 1, b2);  // dK,dV: dP^T = V dO^T   dQ: dP = dO V^T
           commit(y_full);
           if (j == it.hi) commit(a_empty);
-          // the accumulators of the previous item must have been read out before the first accumulation
-          if (j == it.lo && k > 0 && !(ok = wait(acc_free, (k - 1) & 1))) break;
+          // the accumulators this item reuses (the previous item's, or in the dQ kernel the one before it) must have
+          // been read out before the first accumulation
+          const int kprev = kDQ ? k - 2 : k - 1;
+          if (j == it.lo && kprev >= 0 && !(ok = wait(acc_free + acc_buf<kDQ>(kprev), acc_phase<kDQ>(kprev)))) break;
           const uint32_t acc0 = j > it.lo ? 1u : 0u;
           if (!kDQ) {
             if (!(ok = wait(p_full, ns & 1))) break;
@@ -428,10 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             if (!(ok = wait(ds_full, ns & 1))) break;
             tc_fence_after_sync();
-            mma_tm(tAcc0, tY, b1, acc0);  // dQ += dS K
+            mma_tm((k & 1) ? tAcc1 : tAcc0, tY, b1, acc0);  // dQ += dS K
           }
           commit(b_empty + st);
-          if (j == it.hi) commit(acc_done);
+          if (j == it.hi) commit(acc_done + acc_buf<kDQ>(k));
         }
       }
       if (leader) umma_commit(mma_final);  // every issued product completes before TMEM is released
@@ -446,12 +457,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tX = tbase + lane_base + kColX, tY = tbase + lane_base + kColY;
     constexpr uint32_t kBarAll = 1;    // named barrier of the 256 elementwise threads
+    // ---- epilogue of the k-th item: its accumulators, scaled, to global memory (fp32).  Every elementwise thread
+    // calls it at the same point; returns false (for all) when a wait failed.
+    auto epilogue = [&](const Item& it, int k) {
+      bool fail = !__all_sync(0xffffffffu, mbar_wait(acc_done + acc_buf<kDQ>(k), acc_phase<kDQ>(k), lim, abort_flag));
+      if (!named_bar_and(kBarAll, 2 * 128, !fail)) return false;
+      tc_fence_after_sync();
+      size_t row_off = 0;
+      bool store = false;
+      if (!kDQ) {
+        const int key_row = it.tile * 128 + r;
+        store = key_row < p.T;
+        row_off = ((static_cast<size_t>(it.b) * p.T + key_row) * p.Hkv + it.g) * 128;
+      } else {
+        const int t = it.tile * p.P + r / p.G;
+        store = r < GP && t < p.T;
+        row_off = ((static_cast<size_t>(it.b) * p.T + t) * p.Hq + it.g * p.G + r % p.G) * 128;
+      }
+#pragma unroll
+      for (int a = 0; a < (kDQ ? 1 : 2); ++a) {
+        float* dst = (a == 0 ? p.dst_a : p.dst_b) + row_off + 64 * h;
+        const float sc = a == 0 ? p.scale_a : 1.f;
+        // dK,dV: dK in accumulator 0, dV in 1; dQ: the item's own buffer
+        const uint32_t col = kDQ ? ((k & 1) ? kColAcc1 : kColAcc0) : (a == 0 ? kColAcc0 : kColAcc1);
+        const uint32_t tacc = tbase + lane_base + col + 64 * h;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t av[32];
+          tmem_ld32(tacc + 32 * c2, av);
+          tmem_ld_wait(av);
+          if (store) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              reinterpret_cast<float4*>(dst + 32 * c2)[w] =
+                  make_float4(__uint_as_float(av[4 * w]) * sc, __uint_as_float(av[4 * w + 1]) * sc,
+                              __uint_as_float(av[4 * w + 2]) * sc, __uint_as_float(av[4 * w + 3]) * sc);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_free + acc_buf<kDQ>(k));
+      return true;
+    };
     int nb = 0, ns = 0;
     bool ok = true;
+    Item pending;          // dQ: the item whose epilogue waits for the next item's first step
+    int pending_k = -1;
+    bool failed = false;   // the same for all 256 threads: set only where a barrier AND has failed for everyone
     for (int k = 0; ok; ++k) {
       const int slot = k & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(sched_full + slot, (k >> 1) & 1, lim, abort_flag));
-      if (!named_bar_and(kBarAll, 2 * 128, ok)) break;
+      if (!named_bar_and(kBarAll, 2 * 128, ok)) {
+        failed = true;
+        break;
+      }
       const int item = sched[slot];
       named_bar_sync(kBarAll, 2 * 128);
       if (threadIdx.x == 0) mbar_arrive(sched_empty + slot);
@@ -470,119 +530,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool row_ok = !kDQ || (r < GP && t_row < p.T);
       const int key_row = it.tile * 128 + r;  // dK,dV: this row's key position
-      for (int j = it.lo; !fail && j <= it.hi; ++j, ++nb, ++ns) {
-        const int st = nb % kStages;
-        // visible columns of this thread's row: one interval [lo_c, hi_c] of the tile's 128 columns
-        int lo_c, hi_c;
-        if (!kDQ) {
-          // columns = packed query rows of Q tile j: c -> position j P + c / G
-          const int t0 = j * p.P;
-          lo_c = p.G * (key_row - t0);
-          hi_c = min(GP, p.G * (p.T - t0)) - 1;
-          if (p.window >= 0) hi_c = min(hi_c, p.G * (key_row + p.window - t0) + p.G - 1);
-        } else {
-          // columns = keys j 128 + c
-          hi_c = row_ok ? t_row - j * 128 : -1;
-          lo_c = p.window < 0 ? INT_MIN / 2 : hi_c - p.window;
-        }
-        const float* vec = sVec + st * 256;  // dK,dV: lse and rowsum of the columns (Q tile j), landed with B
-        if (!kDQ) {
-          fail = !__all_sync(0xffffffffu, mbar_wait(b_full + st, (nb / kStages) & 1, lim, abort_flag));
-          if (fail) break;
-        }
-        fail = !__all_sync(0xffffffffu, mbar_wait(x_full, ns & 1, lim, abort_flag));
-        if (fail) break;
-        tc_fence_after_sync();
-        // ---- probabilities: P = 2^(X - lse) on the visible columns, 0 elsewhere
-        float pv[2][32];
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int c0 = 64 * h + 32 * c2;
-          uint32_t sv[32];
-          tmem_ld32(tX + c0, sv);
-          tmem_ld_wait(sv);
-          const uint32_t vis = interval_mask(lo_c, hi_c, c0);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float l = kDQ ? lse_r : vec[c0 + c];
-            pv[c2][c] = ((vis >> c) & 1u) ? ex2_approx(__uint_as_float(sv[c]) - l) : 0.f;
+      // Every thread runs every step of the item (a thread whose wait failed skips the work), so that all of them
+      // meet the barrier of the deferred epilogue after the first step.
+      for (int j = it.lo; j <= it.hi; ++j, ++nb, ++ns) {
+        if (!fail) {
+          const int st = nb % kStages;
+          // visible columns of this thread's row: one interval [lo_c, hi_c] of the tile's 128 columns
+          int lo_c, hi_c;
+          if (!kDQ) {
+            // columns = packed query rows of Q tile j: c -> position j P + c / G
+            const int t0 = j * p.P;
+            lo_c = p.G * (key_row - t0);
+            hi_c = min(GP, p.G * (p.T - t0)) - 1;
+            if (p.window >= 0) hi_c = min(hi_c, p.G * (key_row + p.window - t0) + p.G - 1);
+          } else {
+            // columns = keys j 128 + c
+            hi_c = row_ok ? t_row - j * 128 : -1;
+            lo_c = p.window < 0 ? INT_MIN / 2 : hi_c - p.window;
           }
-          if (!kDQ) {  // P^T is an operand of dV += P^T dO: bf16 pairs over the S^T columns just read
-            uint32_t pk[16];
+          const float* vec = sVec + st * 256;  // dK,dV: lse and rowsum of the columns (Q tile j), landed with B
+          if (!kDQ) fail = !__all_sync(0xffffffffu, mbar_wait(b_full + st, (nb / kStages) & 1, lim, abort_flag));
+          if (!fail) fail = !__all_sync(0xffffffffu, mbar_wait(x_full, ns & 1, lim, abort_flag));
+          if (!fail) {
+            tc_fence_after_sync();
+            // ---- probabilities: P = 2^(X - lse) on the visible columns, 0 elsewhere
+            float pv[2][32];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[c2][2 * c], pv[c2][2 * c + 1]);
-            tmem_st16(tX + 64 * h + 16 * c2, pk);
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int c0 = 64 * h + 32 * c2;
+              uint32_t sv[32];
+              tmem_ld32(tX + c0, sv);
+              tmem_ld_wait(sv);
+              const uint32_t vis = interval_mask(lo_c, hi_c, c0);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const float l = kDQ ? lse_r : vec[c0 + c];
+                pv[c2][c] = ((vis >> c) & 1u) ? ex2_approx(__uint_as_float(sv[c]) - l) : 0.f;
+              }
+              if (!kDQ) {  // P^T is an operand of dV += P^T dO: bf16 pairs over the S^T columns just read
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pv[c2][2 * c], pv[c2][2 * c + 1]);
+                tmem_st16(tX + 64 * h + 16 * c2, pk);
+              }
+            }
+            if (!kDQ) {
+              tmem_st_wait();
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(p_full);
+            }
+            // ---- dS = P (dP - rowsum), bf16 pairs over the dP columns just read
+            fail = !__all_sync(0xffffffffu, mbar_wait(y_full, ns & 1, lim, abort_flag));
+            if (!fail) {
+              tc_fence_after_sync();
+#pragma unroll
+              for (int c2 = 0; c2 < 2; ++c2) {
+                const int c0 = 64 * h + 32 * c2;
+                uint32_t dv[32];
+                tmem_ld32(tY + c0, dv);
+                tmem_ld_wait(dv);
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                  const float d0 = kDQ ? dr_r : vec[128 + c0 + 2 * c];
+                  const float d1 = kDQ ? dr_r : vec[128 + c0 + 2 * c + 1];
+                  pk[c] = pack_bf16x2(pv[c2][2 * c] * (__uint_as_float(dv[2 * c]) - d0),
+                                      pv[c2][2 * c + 1] * (__uint_as_float(dv[2 * c + 1]) - d1));
+                }
+                tmem_st16(tY + 64 * h + 16 * c2, pk);
+              }
+              tmem_st_wait();
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(ds_full);
+            }
           }
         }
-        if (!kDQ) {
-          tmem_st_wait();
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(p_full);
-        }
-        // ---- dS = P (dP - rowsum), bf16 pairs over the dP columns just read
-        fail = !__all_sync(0xffffffffu, mbar_wait(y_full, ns & 1, lim, abort_flag));
-        if (fail) break;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int c0 = 64 * h + 32 * c2;
-          uint32_t dv[32];
-          tmem_ld32(tY + c0, dv);
-          tmem_ld_wait(dv);
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float d0 = kDQ ? dr_r : vec[128 + c0 + 2 * c];
-            const float d1 = kDQ ? dr_r : vec[128 + c0 + 2 * c + 1];
-            pk[c] = pack_bf16x2(pv[c2][2 * c] * (__uint_as_float(dv[2 * c]) - d0),
-                                pv[c2][2 * c + 1] * (__uint_as_float(dv[2 * c + 1]) - d1));
-          }
-          tmem_st16(tY + 64 * h + 16 * c2, pk);
-        }
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ds_full);
-      }
-      if (!named_bar_and(kBarAll, 2 * 128, !fail)) break;
-      // ---- epilogue: the accumulators, scaled, to global memory (fp32)
-      fail = !__all_sync(0xffffffffu, mbar_wait(acc_done, k & 1, lim, abort_flag));
-      if (!named_bar_and(kBarAll, 2 * 128, !fail)) break;
-      tc_fence_after_sync();
-      size_t row_off = 0;
-      bool store = false;
-      if (!kDQ) {
-        store = key_row < p.T;
-        row_off = ((static_cast<size_t>(it.b) * p.T + key_row) * p.Hkv + it.g) * 128;
-      } else {
-        const int t = it.tile * p.P + r / p.G;
-        store = r < GP && t < p.T;
-        row_off = ((static_cast<size_t>(it.b) * p.T + t) * p.Hq + it.g * p.G + r % p.G) * 128;
-      }
-#pragma unroll
-      for (int a = 0; a < (kDQ ? 1 : 2); ++a) {
-        float* dst = (a == 0 ? p.dst_a : p.dst_b) + row_off + 64 * h;
-        const float sc = a == 0 ? p.scale_a : 1.f;
-        const uint32_t tacc = tbase + lane_base + (a == 0 ? kColAcc0 : kColAcc1) + 64 * h;
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t av[32];
-          tmem_ld32(tacc + 32 * c2, av);
-          tmem_ld_wait(av);
-          if (store) {
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-              reinterpret_cast<float4*>(dst + 32 * c2)[w] =
-                  make_float4(__uint_as_float(av[4 * w]) * sc, __uint_as_float(av[4 * w + 1]) * sc,
-                              __uint_as_float(av[4 * w + 2]) * sc, __uint_as_float(av[4 * w + 3]) * sc);
-          }
+        if (kDQ && j == it.lo && pending_k >= 0) {
+          // the previous item's epilogue, while the tensor core works on this item's next step
+          if (!named_bar_and(kBarAll, 2 * 128, !fail) || !epilogue(pending, pending_k)) fail = true;
+          pending_k = -1;
         }
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_free);
+      if (!named_bar_and(kBarAll, 2 * 128, !fail)) {
+        failed = true;
+        break;
+      }
+      if (kDQ) {
+        pending = it;
+        pending_k = k;
+      } else if (!epilogue(it, k)) {
+        failed = true;
+        break;
+      }
     }
+    if (kDQ && !failed && pending_k >= 0) epilogue(pending, pending_k);
   }
 
   // ------------------------------------------------------------------ teardown
