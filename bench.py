@@ -412,14 +412,15 @@ def run_ours(args, ws, rank, local):
 
     sections = set(args.sections.split(","))
 
-    # ---- headline: the long-context step, with clocks sampled during its timed region
-    w = LONG
+    # ---- headline: the long-context step (another workload or the fp8 path only for profiling runs), with clocks
+    # sampled during its timed region
+    w = {"long": LONG, "depth12": DEPTH12, "gqa": GQA, "tiny": TINY}[args.workload]
     clocks = ClockSampler(local)
     clocks.start()
     dist_barrier(ws)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    head, step_ms, layers, wsp = prefill_section(nc, w, dev, flush, args.steps, args.warmup)
+    head, step_ms, layers, wsp = prefill_section(nc, w, dev, flush, args.steps, args.warmup, fp8=args.fp8)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     clk = clocks.stop(t_wall0, t_wall1)
@@ -650,7 +651,8 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": LONG_WORKLOAD,
+            "config": {"workload": LONG_WORKLOAD if w is LONG and not args.fp8 else
+                       head["workload"] + (" (e4m3 scores)" if args.fp8 else "") + " [profiling run, not the headline]",
                        "l2": "512 MiB write before every timed step, outside the timed events",
                        "timing": "each step replayed from a CUDA graph of its four kernels; kernel times for the "
                                  "roofline from CUDA events around each kernel in eager steps",
@@ -687,6 +689,9 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["long", "depth12", "gqa", "tiny"], default="long",
+                    help="workload of the headline step (long-context unless a profiling run asks for another)")
+    ap.add_argument("--fp8", action="store_true", help="headline step on the e4m3 path (profiling runs)")
     ap.add_argument("--sections", default=ALL_SECTIONS,
                     help="comma-separated sections timed after the headline step (default: all of " + ALL_SECTIONS + ")")
     args = ap.parse_args()
