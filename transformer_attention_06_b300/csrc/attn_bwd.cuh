@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_empty = bars + kBarBEmpty;      // [kStages] every product reading the stage done   MMA -> TMA
   uint64_t* x_full = bars + kBarXFull;        // X = A1 B1^T in TMEM                              MMA -> ew
   uint64_t* y_full = bars + kBarYFull;        // Y = A2 B2^T in TMEM                              MMA -> ew
-  uint64_t* p_full = bars + kBarPFull;        // P^T written over X (dK,dV; one arrival per warp) ew -> MMA
+  uint64_t* p_full = bars + kBarPFull;        // X consumed: P^T over it (dK,dV) or read (dQ); per warp ew -> MMA
   uint64_t* ds_full = bars + kBarDsFull;      // dS written over Y (one arrival per warp)         ew -> MMA
   uint64_t* acc_done = bars + kBarAccDone;    // [2] the item's last accumulation complete        MMA -> ew
   uint64_t* acc_free = bars + kBarAccFree;    // [2] accumulators read by the epilogue (per warp) ew -> MMA
@@ -414,35 +414,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (item < 0) break;
         const Item it = decode_item<kDQ>(p, item);
         if (!(ok = wait(a_full, k & 1))) break;
+        // Products of a step (B stage st: b1 = Q' / K tile, b2 = dO / V tile):
+        //   X = A1 b1^T (dK,dV: S^T = K Q'^T; dQ: S = Q' K^T),  Y = A2 b2^T (dP^T = V dO^T; dP = dO V^T),
+        //   dK,dV: dV += P^T dO (A = X) and dK += dS^T Q' (A = Y);  dQ: dQ += dS K (A = Y).
+        // The next step's X goes in as soon as this step's X has been consumed (P^T written over it, or read), and
+        // its Y right after the product that reads this step's dS: the tensor core runs them while the elementwise
+        // warps work on this step's dS and the next step's P.  Products of one thread run in issue order, so a
+        // product that overwrites X or Y follows the one that reads it.
+        if (!(ok = wait(b_full + nb % kStages, (nb / kStages) & 1))) break;
+        tc_fence_after_sync();
+        mma_kk(tX, 0, 2 * (nb % kStages));
+        commit(x_full);
+        mma_kk(tY, 1, 2 * (nb % kStages) + 1);
+        commit(y_full);
+        if (it.lo == it.hi) commit(a_empty);
         for (int j = it.lo; j <= it.hi; ++j, ++nb, ++ns) {
-          const int st = nb % kStages;
+          const int st = nb % kStages, st1 = (nb + 1) % kStages;
           const int b1 = 2 * st, b2 = 2 * st + 1;
-          if (!(ok = wait(b_full + st, (nb / kStages) & 1))) break;
-          tc_fence_after_sync();
-          mma_kk(tX, 0, b1);  // dK,dV: S^T = K Q'^T     dQ: S = Q' K^T
-          commit(x_full);
-          mma_kk(tY, 1, b2);  // dK,dV: dP^T = V dO^T   dQ: dP = dO V^T
-          commit(y_full);
-          if (j == it.hi) commit(a_empty);
+          const bool more = j < it.hi;
           // the accumulators this item reuses (the previous item's, or in the dQ kernel the one before it) must have
           // been read out before the first accumulation
           const int kprev = kDQ ? k - 2 : k - 1;
           if (j == it.lo && kprev >= 0 && !(ok = wait(acc_free + acc_buf<kDQ>(kprev), acc_phase<kDQ>(kprev)))) break;
           const uint32_t acc0 = j > it.lo ? 1u : 0u;
-          if (!kDQ) {
-            if (!(ok = wait(p_full, ns & 1))) break;
-            tc_fence_after_sync();
-            mma_tm(tAcc1, tX, b2, acc0);  // dV += P^T dO
-            if (!(ok = wait(ds_full, ns & 1))) break;
-            tc_fence_after_sync();
-            mma_tm(tAcc0, tY, b1, acc0);  // dK += dS^T Q'
-          } else {
-            if (!(ok = wait(ds_full, ns & 1))) break;
-            tc_fence_after_sync();
-            mma_tm((k & 1) ? tAcc1 : tAcc0, tY, b1, acc0);  // dQ += dS K
+          if (!(ok = wait(p_full, ns & 1))) break;  // X consumed
+          if (more && !(ok = wait(b_full + st1, ((nb + 1) / kStages) & 1))) break;
+          tc_fence_after_sync();
+          if (!kDQ) mma_tm(tAcc1, tX, b2, acc0);  // dV += P^T dO
+          if (more) {
+            mma_kk(tX, 0, 2 * st1);  // next X
+            commit(x_full);
           }
+          if (!(ok = wait(ds_full, ns & 1))) break;
+          tc_fence_after_sync();
+          mma_tm(kDQ ? ((k & 1) ? tAcc1 : tAcc0) : tAcc0, tY, b1, acc0);  // dK += dS^T Q'  /  dQ += dS K
           commit(b_empty + st);
-          if (j == it.hi) commit(acc_done + acc_buf<kDQ>(k));
+          if (more) {
+            mma_kk(tY, 1, 2 * st1 + 1);  // next Y
+            commit(y_full);
+            if (j + 1 == it.hi) commit(a_empty);
+          } else {
+            commit(acc_done + acc_buf<kDQ>(k));
+          }
         }
       }
       if (leader) umma_commit(mma_final);  // every issued product completes before TMEM is released
@@ -574,12 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st16(tX + 64 * h + 16 * c2, pk);
               }
             }
-            if (!kDQ) {
-              tmem_st_wait();
-              tc_fence_before_sync();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(p_full);
-            }
+            // X consumed (dK,dV: P^T written over it; dQ: read into registers): the next step's X may go in
+            if (!kDQ) tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
             // ---- dS = P (dP - rowsum), bf16 pairs over the dP columns just read
             fail = !__all_sync(0xffffffffu, mbar_wait(y_full, ns & 1, lim, abort_flag));
             if (!fail) {

@@ -8,8 +8,9 @@
 //
 // Tiling.  A Q tile is 128 MMA rows: P = 128 / G consecutive query positions times the G query heads of kv head g
 // (row r = position r / G, head r % G), so every K/V tile brought in by TMA serves the whole GQA group.  A work item
-// is two consecutive Q tiles (A and B) of one (b, g): every K/V tile is loaded once for both (or a single tile, when
-// pairs would leave SMs without an item).  Keys are processed in tiles of 128; a Q tile only visits the key tiles
+// is two consecutive Q tiles (A and B) of one (b, g): every K/V tile is loaded once for both.  When pairs would
+// leave SMs without an item, an item is a single Q tile whose key range runs as two chains A and B (first and second
+// half of its key tiles, visited alternately) whose partial sums the epilogue adds.  Keys are processed in tiles of 128; a Q tile only visits the key tiles
 // that intersect its causal / window band, and only tiles that straddle the band edge pay for the element mask.
 //
 // Persistent grid: one CTA per SM takes work items from a global counter (zeroed by the prologue kernel), the
@@ -156,12 +157,20 @@ __device__ __forceinline__ QRange q_range(const Params& p, int t0, int p0) {
   return q;
 }
 
+// A work item walks its key tiles in rounds, one K/V tile per round.  Two-tile items (split = false): round i visits
+// key tile lo + i, which Q tile X uses when it lies in X's range.  Single-tile items (split = true): the tile's key
+// range is cut into two halves run as two chains -- chain A over the first na tiles, chain B over the last nb --
+// visited alternately (A, B, A, B, ..., then A's last tile when na > nb), so that each chain's softmax overlaps the
+// other chain's products.  Without a running maximum the partial sums of the two chains add up exactly: the epilogue
+// returns (O_A + O_B) / (l_A + l_B).
 struct Item {
   int b, g;
   QRange qa, qb;
   int lo, hi;   // union of the two key-tile ranges
+  int na, nb;   // split: rounds of chain A and of chain B
   int tail;     // key tile read from the zero-padded V tail copy (-1: none)
   bool valid;   // false: the sequence's cache length is out of range; nothing is stored
+  bool split;
 };
 
 __device__ __forceinline__ Item decode_item(const Params& p, int item) {
@@ -179,8 +188,37 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item) {
   it.qb = q_range(p, p.tiles_per_item == 2 ? pair * 2 * p.P + p.P : p.T, p0);
   it.lo = it.qa.lo;
   it.hi = it.qb.n > 0 ? max(it.qa.hi, it.qb.hi) : it.qa.hi;
+  // The statistics launch of the backward keeps one chain per item: its row sums then add the key tiles in the same
+  // order whether the items are pairs or single tiles, so the gradients do not depend on the batch composition.
+  it.split = p.tiles_per_item == 1 && p.lse == nullptr;
+  it.na = (it.qa.n + 1) / 2;
+  it.nb = it.qa.n / 2;
   it.tail = p.pos0 != nullptr ? (p0 + p.T - 1) / kBlockN : -1;
   return it;
+}
+
+__device__ __forceinline__ int n_rounds(const Item& it) { return it.hi - it.lo + 1; }
+
+// key tile of round i
+__device__ __forceinline__ int round_tile(const Item& it, int i) {
+  if (!it.split) return it.lo + i;
+  return i < 2 * it.nb ? it.lo + ((i & 1) ? it.na : 0) + (i >> 1) : it.lo + i - it.nb;
+}
+
+// chain (Q tile) x takes part in round i
+__device__ __forceinline__ bool in_chain(const Item& it, int x, int i) {
+  if (it.split) return x == 0 ? (i >= 2 * it.nb || (i & 1) == 0) : (i < 2 * it.nb && (i & 1) == 1);
+  const QRange& q = x == 0 ? it.qa : it.qb;
+  const int j = it.lo + i;
+  return q.n > 0 && j >= q.lo && j <= q.hi;
+}
+
+// chain x has at least one round, and its first round
+__device__ __forceinline__ bool chain_active(const Item& it, int x) {
+  return it.split ? (x == 0 ? it.na > 0 : it.nb > 0) : (x == 0 ? it.qa.n > 0 : it.qb.n > 0);
+}
+__device__ __forceinline__ int first_round(const Item& it, int x) {
+  return it.split ? x : (x == 0 ? it.qa.lo : it.qb.lo) - it.lo;
 }
 
 // kFp8: qn and kn are e4m3 (scores on tcgen05 kind::f8f6f4); otherwise bf16 (kind::f16).  P and V are bf16 in both.
@@ -284,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmO);
       if (p.pos0 != nullptr) tma_prefetch_desc(&tmVt);
       // Items fetched so far live in a 2-slot ring (the same slots the consumers read).  Three cursors walk the
-      // item sequence: Q (item iq), K (item ik, tile jk), V (item iv, tile jv); kt / vt count the K / V tiles
+      // item sequence: Q (item iq), K (item ik, round jk), V (item iv, round jv); kt / vt count the K / V tiles
       // loaded over all items (ring positions).
       Item items[2];
       int nfetched = 0;
@@ -306,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             done = true;
           } else {
             items[slot] = decode_item(p, item);
-            jk = items[slot].lo;
-            if (nfetched == iv) jv = items[slot].lo;
+            jk = 0;
+            if (nfetched == iv) jv = 0;
             ++nfetched;
           }
           progress = true;
@@ -317,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Item& it = items[iq & 1];
           // past T the box reads as zeros (still full bytes)
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const int t0 = x == 0 ? it.qa.t0 : it.qb.t0;
+          for (int x = 0; x < 2; ++x) {  // a split item's two chains use the same Q tile
+            const int t0 = x == 0 || it.split ? it.qa.t0 : it.qb.t0;
             mbar_arrive_expect_tx(q_full + x, q_bytes);
             tma_load_4d(sQ + x * L::kQKBytes, &tmQ, q_full + x, 0, it.g * p.G, t0, it.b);
             if (!kFp8) tma_load_4d(sQ + x * L::kQKBytes + kHalfBytes, &tmQ, q_full + x, 64, it.g * p.G, t0, it.b);
@@ -331,11 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Item& it = items[ik & 1];
           const int st = kt % kKStages;
           uint8_t* dk = sK + st * L::kQKBytes;
+          const int row = round_tile(it, jk) * kBlockN;
           mbar_arrive_expect_tx(k_full + st, L::kQKBytes);
-          tma_load_4d(dk, &tmK, k_full + st, 0, it.g, jk * kBlockN, it.b);
-          if (!kFp8) tma_load_4d(dk + kHalfBytes, &tmK, k_full + st, 64, it.g, jk * kBlockN, it.b);
+          tma_load_4d(dk, &tmK, k_full + st, 0, it.g, row, it.b);
+          if (!kFp8) tma_load_4d(dk + kHalfBytes, &tmK, k_full + st, 64, it.g, row, it.b);
           ++kt;
-          if (++jk > it.hi) ++ik;  // the next item's first tile is set when it is fetched
+          if (++jk == n_rounds(it)) ++ik;  // the next item's first round is set when it is fetched
           progress = true;
         }
         // next V tile
@@ -347,15 +386,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(v_full + st, kTileBytes);
             // the tile holding the last key of a chunked prefill comes from its zero-padded copy: cache rows past
             // the chunk may hold anything, and P = 0 times a NaN would still poison O
-            const bool from_tail = jv == it.tail;
+            const int jt = round_tile(it, jv);
+            const bool from_tail = jt == it.tail;
             const CUtensorMap* mv = from_tail ? &tmVt : &tmV;
-            const int row = from_tail ? 0 : jv * kBlockN;
+            const int row = from_tail ? 0 : jt * kBlockN;
             tma_load_4d(dv, mv, v_full + st, 0, it.g, row, it.b);
             tma_load_4d(dv + kHalfBytes, mv, v_full + st, 64, it.g, row, it.b);
             ++vt;
-            if (++jv > it.hi) {
+            if (++jv == n_rounds(it)) {
               ++iv;
-              if (iv < nfetched) jv = items[iv & 1].lo;
+              jv = 0;
             }
             progress = true;
           }
@@ -446,42 +486,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) mbar_arrive(sched_empty + slot);
         if (item < 0) break;
         const Item it = decode_item(p, item);
-        const QRange q = x == 0 ? it.qa : it.qb;
-        const int lo_x = q.n > 0 ? q.lo : INT_MAX, hi_x = q.n > 0 ? q.hi : INT_MIN;
+        const bool active = chain_active(it, x);
+        const int first = first_round(it, x), nr = n_rounds(it);
         // Both issuers wait for every Q, K and V buffer of the item to land -- also the ones their own tile does not
         // use -- before releasing it: the release barriers count one commit from each issuer per fill, and an
         // issuer that ran ahead would otherwise commit twice within one fill.
         if (!(ok = wait(q_full + x, k & 1))) break;
         if (!(ok = wait(k_full + kv % kKStages, (kv / kKStages) & 1))) break;
-        if (lo_x == it.lo) {
+        if (in_chain(it, x, 0)) {
           tc_fence_after_sync();
           issue_s(kv % kKStages);
         }
         commit(k_empty + kv % kKStages);
-        for (int j = it.lo; ok && j <= it.hi; ++j, ++kv) {
+        for (int i = 0; ok && i < nr; ++i, ++kv) {
           const int vst = kv % kVStages, kst1 = (kv + 1) % kKStages;
-          const bool more = j < it.hi;
-          // Every wait of the round comes first, so that P.V(j) and the next S go into the tensor core back to back
-          // (a gap between them lets its pipeline drain).  K(j+1) has normally landed a round earlier.
+          const bool more = i + 1 < nr;
+          const bool pv = in_chain(it, x, i);
+          const bool s_next = more && in_chain(it, x, i + 1);
+          if (it.split && !pv) {
+            // The other chain's round of a split item: this chain's next S goes in as soon as its K tile has landed;
+            // the V tile of the round, which only the other chain reads, is waited for (the release barrier counts
+            // one commit per issuer and fill) and released afterwards.
+            if (more) {
+              if (!(ok = wait(k_full + kst1, ((kv + 1) / kKStages) & 1))) break;
+              tc_fence_after_sync();
+              if (s_next) issue_s(kst1);
+              commit(k_empty + kst1);
+            }
+            if (!(ok = wait(v_full + vst, (kv / kVStages) & 1))) break;
+            commit(v_empty + vst);
+            continue;
+          }
+          // Every wait of the round comes first, so that P.V and the next S go into the tensor core back to back (a
+          // gap between them lets its pipeline drain).  The next K tile has normally landed a round earlier.
           if (!(ok = wait(v_full + vst, (kv / kVStages) & 1))) break;
           if (more && !(ok = wait(k_full + kst1, ((kv + 1) / kKStages) & 1))) break;
-          const bool pv = j >= lo_x && j <= hi_x;
+          // A tile this issuer does not read is released at once (its commit tracks only earlier products), not
+          // after this round's P.V: in a split item the chain's softmax would otherwise hold the other chain's K tile.
+          if (!pv) commit(v_empty + vst);
+          if (more && !s_next) commit(k_empty + kst1);
           if (pv) {
-            if (j == lo_x && nit > 0 && !(ok = wait(o_free + x, (nit - 1) & 1))) break;
+            if (i == first && nit > 0 && !(ok = wait(o_free + x, (nit - 1) & 1))) break;
             if (!(ok = wait(p_full + x, ns & 1))) break;
           }
           tc_fence_after_sync();
-          if (pv) {  // O_X += P_X V_j
-            issue_pv(vst, j > lo_x ? 1u : 0u);
+          if (pv) {  // O_X += P_X V (the key tile of round i)
+            issue_pv(vst, i > first ? 1u : 0u);
             ++ns;
           }
-          if (more && j + 1 >= lo_x && j + 1 <= hi_x) issue_s(kst1);  // S_X = Q_X K_{j+1}^T
-          commit(v_empty + vst);
-          if (more) commit(k_empty + kst1);
+          if (s_next) issue_s(kst1);  // S_X = Q_X K^T (the key tile of round i + 1)
+          if (pv) commit(v_empty + vst);
+          if (s_next) commit(k_empty + kst1);
         }
         if (!ok) break;
         commit(q_empty);
-        nit += q.n > 0 ? 1 : 0;
+        nit += active ? 1 : 0;
       }
       if (leader) umma_commit(mma_final + x);  // all issued MMAs complete before TMEM is released
       __syncwarp();
@@ -512,11 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every barrier of the 256 softmax threads, each barrier ANDs the threads' status, and the warps leave the
       // loops together, right after a barrier, when any of them failed.
       bool fail = false;
-      for (int j = it.lo; ok && j <= it.hi; ++j) {
+      const int nr = n_rounds(it);
+      for (int i = 0; ok && i < nr; ++i) {
+        const int j = round_tile(it, i);
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          const QRange q = x == 0 ? it.qa : it.qb;
-          if (q.n == 0 || j < q.lo || j > q.hi) continue;
+          if (!in_chain(it, x, i)) continue;
+          const QRange q = x == 0 || it.split ? it.qa : it.qb;
           const uint32_t tS = tbase + lane_base + kColS + x * 128;
           const int t = q.a0 + tpos;  // position of this row's query
           if (!fail) fail = !mbar_wait(s_full + x, ns[x] & 1, lim, abort_flag);
@@ -575,17 +636,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // All 256 threads agree on the item's outcome before the epilogues use the exchange area.
       if (!named_bar_and(kBarAll, 2 * kSoftThreads, ok && !fail)) break;
-      // ---- epilogues: O / l once the last P.V of each Q tile has completed
+      // ---- epilogues: O / l once the last P.V of each Q tile has completed; a split item has one epilogue,
+      // (O_A + O_B) / (l_A + l_B)
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
+        if (!chain_active(it, x) || (it.split && x == 1)) continue;
         const QRange q = x == 0 ? it.qa : it.qb;
-        if (q.n == 0) continue;
+        const bool merge = it.split && it.nb > 0;  // add chain B's partial sums
         const uint32_t tO = tbase + lane_base + kColO + x * 128;
+        const uint32_t tOB = tbase + lane_base + kColO + 128;
         const bool row_in_box = r < p.G * p.P;  // rows past G * P belong to no query
         fail = !mbar_wait(o_done + x, (ns[x] - 1) & 1, lim, abort_flag);
+        if (merge && !fail) fail = !mbar_wait(o_done + 1, (ns[1] - 1) & 1, lim, abort_flag);
         fail = !__all_sync(0xffffffffu, !fail);
         float* lx = xch;  // [2 halves][128] row sums
-        if (!fail) lx[h * 128 + r] = l[x];
+        if (!fail) lx[h * 128 + r] = merge ? l[0] + l[1] : l[x];
         // the staging tile is free once the previous tile's TMA store has read it
         if (threadIdx.x == 0) bulk_wait_read_all();
         if (!named_bar_and(kBarAll, 2 * kSoftThreads, !fail)) { ok = false; break; }
@@ -607,7 +672,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t ov[32];
           tmem_ld32(tO + 64 * h + 32 * c2, ov);
-          tmem_ld_wait(ov);
+          if (merge) {
+            uint32_t ob[32];
+            tmem_ld32(tOB + 64 * h + 32 * c2, ob);
+            tmem_ld_wait(ov);
+            tmem_ld_wait(ob);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) + __uint_as_float(ob[c]));
+          } else {
+            tmem_ld_wait(ov);
+          }
           if (dorow != nullptr) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
@@ -636,7 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();  // the generic-proxy writes above become visible to the TMA store
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(o_free + x);  // the MMA may start the next item's P.V into O_X
+        if (lane == 0) {  // the MMA may start the next item's P.V into O_X (and O_B)
+          mbar_arrive(o_free + x);
+          if (merge) mbar_arrive(o_free + 1);
+        }
         if (p.drow != nullptr) xch[256 + h * 128 + r] = dpart;
         named_bar_sync(kBarAll, 2 * kSoftThreads);  // staging tile written; the row-sum area is free again
         if (p.lse != nullptr && h == 0) {

@@ -48,7 +48,7 @@ __device__ __forceinline__ float ex2_approx(float x) {  // MUFU.EX2; ex2(-inf) =
   return y;
 }
 
-// Packed pairs of fp32 (one 64-bit register pair): a . b + c and a + b for both lanes in one instruction.
+// Packed pairs of fp32 (one 64-bit register pair): a . b + c, a . b and a + b for both lanes in one instruction.
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -60,6 +60,11 @@ __device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {

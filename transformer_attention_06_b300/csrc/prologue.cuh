@@ -18,29 +18,39 @@ namespace nc {
 
 // Rotates the 8 pairs held in (lo, hi) -- elements [8kq, 8kq+8) and [64+8kq, 64+8kq+8) of a 128-wide head
 // vector -- and normalises by the RMS of the whole vector (reduced over the 8-lane group `gmask`), times `scale`.
+// Two neighbouring elements travel together through packed fp32 pairs (f32x2: one instruction for both), so the
+// rotation, the sum of squares and the scaling cost half the instructions of scalar code.
 __device__ __forceinline__ void rope_norm_slices(const uint4& lo, const uint4& hi, const float (&c)[8],
                                                  const float (&s)[8], unsigned gmask, float scale,
                                                  float (&y1)[8], float (&y2)[8]) {
   const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w};
   const uint32_t b[4] = {hi.x, hi.y, hi.z, hi.w};
-  float ss = 0.f;
+  uint64_t r1[4], r2[4];
+  uint64_t ss2 = 0ull;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float x1 = (i & 1) ? bf16_hi(a[i >> 1]) : bf16_lo(a[i >> 1]);
-    const float x2 = (i & 1) ? bf16_hi(b[i >> 1]) : bf16_lo(b[i >> 1]);
-    y1[i] = fmaf(x1, c[i], x2 * s[i]);
-    y2[i] = fmaf(x2, c[i], -(x1 * s[i]));
-    ss = fmaf(y1[i], y1[i], ss);
-    ss = fmaf(y2[i], y2[i], ss);
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t x1 = f32x2(bf16_lo(a[i]), bf16_hi(a[i]));
+    const uint64_t x2 = f32x2(bf16_lo(b[i]), bf16_hi(b[i]));
+    const uint64_t cc = f32x2(c[2 * i], c[2 * i + 1]);
+    const uint64_t sp = f32x2(s[2 * i], s[2 * i + 1]);
+    const uint64_t sn = f32x2(-s[2 * i], -s[2 * i + 1]);
+    r1[i] = fma_f32x2(x1, cc, mul_f32x2(x2, sp));   // x1 c + x2 s
+    r2[i] = fma_f32x2(x2, cc, mul_f32x2(x1, sn));   // x2 c - x1 s
+    ss2 = fma_f32x2(r1[i], r1[i], ss2);
+    ss2 = fma_f32x2(r2[i], r2[i], ss2);
   }
+  float s0, s1;
+  f32x2_split(ss2, s0, s1);
+  float ss = s0 + s1;
   ss += __shfl_xor_sync(gmask, ss, 1);
   ss += __shfl_xor_sync(gmask, ss, 2);
   ss += __shfl_xor_sync(gmask, ss, 4);
   const float inv = rsqrtf(ss * (1.0f / 128.0f) + kRmsEps) * scale;
+  const uint64_t inv2 = f32x2(inv, inv);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    y1[i] *= inv;
-    y2[i] *= inv;
+  for (int i = 0; i < 4; ++i) {
+    f32x2_split(mul_f32x2(r1[i], inv2), y1[2 * i], y1[2 * i + 1]);
+    f32x2_split(mul_f32x2(r2[i], inv2), y2[2 * i], y2[2 * i + 1]);
   }
 }
 
