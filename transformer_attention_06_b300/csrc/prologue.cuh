@@ -75,15 +75,33 @@ __device__ __forceinline__ void store_head(void* dst, int kq, const float (&y1)[
   }
 }
 
+// The first round of rope_norm_token: slices kq and kq + 8 of heads 0..3 of the token's list of Hq q heads followed
+// by its Hkv k heads.  It depends on nothing but the token, so callers issue it before computing the position's
+// cos / sin (and, in the chunked prefill, before the cache length has arrived).
+__device__ __forceinline__ void load_first_heads(const __nv_bfloat16* __restrict__ q,
+                                                 const __nv_bfloat16* __restrict__ k, int Hq, int Hkv, int kq,
+                                                 uint4 (&lo)[4], uint4 (&hi)[4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (u < Hq + Hkv) {
+      const uint4* p = reinterpret_cast<const uint4*>(u < Hq ? q + u * 128 : k + (u - Hq) * 128);
+      lo[u] = __ldg(p + kq);
+      hi[u] = __ldg(p + 8 + kq);
+    }
+  }
+}
+
 // The Hq q heads then the Hkv k heads of one token (q, k, qn, kn point at the token's head 0), in rounds of four
 // heads whose loads are issued one round ahead: while a round is rotated, normalised and stored, the next round's
-// sixteen 16-byte loads per lane are in flight.  OutT = __nv_bfloat16 writes bf16 rows of 256 bytes; OutT = uint8_t
-// writes e4m3 rows of 128 bytes (the values times the scale, rounded to nearest even).
+// sixteen 16-byte loads per lane are in flight.  (lo0, hi0) hold the first round, from load_first_heads.  OutT =
+// __nv_bfloat16 writes bf16 rows of 256 bytes; OutT = uint8_t writes e4m3 rows of 128 bytes (the values times the
+// scale, rounded to nearest even).
 template <typename OutT>
 __device__ __forceinline__ void rope_norm_token(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                                                 OutT* __restrict__ qn, OutT* __restrict__ kn, int Hq, int Hkv, int kq,
                                                 const float (&c)[8], const float (&s)[8], unsigned gmask,
-                                                float q_scale, float k_scale) {
+                                                float q_scale, float k_scale, const uint4 (&lo0)[4],
+                                                const uint4 (&hi0)[4]) {
   constexpr bool kE4m3 = sizeof(OutT) == 1;
   const int H = Hq + Hkv;
   auto src = [&](int i) {
@@ -92,10 +110,8 @@ __device__ __forceinline__ void rope_norm_token(const __nv_bfloat16* __restrict_
   uint4 lo[2][4], hi[2][4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    if (u < H) {
-      lo[0][u] = __ldg(src(u) + kq);
-      hi[0][u] = __ldg(src(u) + 8 + kq);
-    }
+    lo[0][u] = lo0[u];
+    hi[0][u] = hi0[u];
   }
   for (int h0 = 0; h0 < H; h0 += 8) {
 #pragma unroll
@@ -128,24 +144,55 @@ __device__ __forceinline__ void rope_norm_token(const __nv_bfloat16* __restrict_
 // Gated value embedding (the catalog pages list value embeddings with a sigmoid gate, in the ResFormer manner; they give
 // no formula, the reading is v' = v + sigmoid(g) ve with one gate logit g per token and kv head): the H value
 // vectors of one token, 16-byte slices kq and kq + 8 of each, mixed in fp32 and rounded to bf16.
+// Four heads per round, all their loads issued before the first store.
 __device__ __forceinline__ void mix_values(const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ ve,
                                            const __nv_bfloat16* __restrict__ gate, __nv_bfloat16* __restrict__ vmix,
                                            int H, int kq) {
-  for (int h = 0; h < H; ++h) {
-    const float g = __bfloat162float(gate[h]);
-    const float a = 1.f / (1.f + expf(-g));
+  for (int h0 = 0; h0 < H; h0 += 4) {
+    uint4 x[4][2], e[4][2];
+    float g[4];
 #pragma unroll
-    for (int i2 = 0; i2 < 2; ++i2) {
-      const int i = h * 16 + kq + 8 * i2;
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(v) + i);
-      const uint4 e = __ldg(reinterpret_cast<const uint4*>(ve) + i);
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, es[4] = {e.x, e.y, e.z, e.w};
-      uint32_t o[4];
+    for (int u = 0; u < 4; ++u) {
+      if (h0 + u < H) {
+        g[u] = __bfloat162float(gate[h0 + u]);
 #pragma unroll
-      for (int w = 0; w < 4; ++w)
-        o[w] = pack_bf16x2(fmaf(a, bf16_lo(es[w]), bf16_lo(xs[w])), fmaf(a, bf16_hi(es[w]), bf16_hi(xs[w])));
-      reinterpret_cast<uint4*>(vmix)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int i2 = 0; i2 < 2; ++i2) {
+          const int i = (h0 + u) * 16 + kq + 8 * i2;
+          x[u][i2] = __ldg(reinterpret_cast<const uint4*>(v) + i);
+          e[u][i2] = __ldg(reinterpret_cast<const uint4*>(ve) + i);
+        }
+      }
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (h0 + u < H) {
+        const float a = 1.f / (1.f + expf(-g[u]));
+#pragma unroll
+        for (int i2 = 0; i2 < 2; ++i2) {
+          const uint32_t xs[4] = {x[u][i2].x, x[u][i2].y, x[u][i2].z, x[u][i2].w};
+          const uint32_t es[4] = {e[u][i2].x, e[u][i2].y, e[u][i2].z, e[u][i2].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            o[w] = pack_bf16x2(fmaf(a, bf16_lo(es[w]), bf16_lo(xs[w])), fmaf(a, bf16_hi(es[w]), bf16_hi(xs[w])));
+          reinterpret_cast<uint4*>(vmix)[(h0 + u) * 16 + kq + 8 * i2] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+}
+
+// Copies n 16-byte words, lane kq of an 8-lane group taking words kq, kq + 8, ..., with eight loads in flight
+// before the stores.  src and dst do not overlap.
+__device__ __forceinline__ void copy_words(uint4* dst, const uint4* src, int n, int kq) {
+  for (int i0 = kq; i0 < n; i0 += 64) {
+    uint4 t[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (i0 + 8 * u < n) t[u] = src[i0 + 8 * u];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (i0 + 8 * u < n) dst[i0 + 8 * u] = t[u];
   }
 }
 
@@ -169,13 +216,16 @@ __global__ void __launch_bounds__(kPrologueThreads)
   const int kq = threadIdx.x & 7;
   if (tok >= BT) return;  // whole 8-lane groups leave together
   const unsigned gmask = 0xFFu << ((threadIdx.x & 31) & ~7);
+  const __nv_bfloat16* qt = q + static_cast<size_t>(tok) * Hq * 128;
+  const __nv_bfloat16* kt = k + static_cast<size_t>(tok) * Hkv * 128;
+  uint4 lo0[4], hi0[4];
+  load_first_heads(qt, kt, Hq, Hkv, kq, lo0, hi0);
   const float pos = static_cast<float>(tok % T);
   float c[8], s[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) rope_cos_sin(pos, tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
-  rope_norm_token(q + static_cast<size_t>(tok) * Hq * 128, k + static_cast<size_t>(tok) * Hkv * 128,
-                  qn + static_cast<size_t>(tok) * Hq * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hq, Hkv, kq, c,
-                  s, gmask, q_scale, k_scale);
+  rope_norm_token(qt, kt, qn + static_cast<size_t>(tok) * Hq * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hq,
+                  Hkv, kq, c, s, gmask, q_scale, k_scale, lo0, hi0);
   if (ve != nullptr)
     mix_values(v + static_cast<size_t>(tok) * Hkv * 128, ve + static_cast<size_t>(tok) * Hkv * 128,
                ve_gate + static_cast<size_t>(tok) * Hkv, vmix + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq);
@@ -209,7 +259,18 @@ __global__ void __launch_bounds__(kPrologueThreads)
     const int tok = blockIdx.x * kPrologueTokensPerBlock + grp;
     if (tok >= B * Tq) return;  // whole 8-lane groups leave together
     const int b = tok / Tq, t = tok - b * Tq;
+    // Everything read from the chunk is independent of the cache length: the first round of q / k heads and the
+    // first value words are requested together with it.
+    const __nv_bfloat16* qt = q + static_cast<size_t>(tok) * Hq * 128;
+    const __nv_bfloat16* kt = k_new + static_cast<size_t>(tok) * Hkv * 128;
+    const uint4* vs = reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(tok) * Hkv * 128);
     const int p0 = __ldg(cache_lens + b);
+    uint4 lo0[4], hi0[4], v0[4];
+    load_first_heads(qt, kt, Hq, Hkv, kq, lo0, hi0);
+    const bool plain_v = ve_new == nullptr;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (plain_v && kq + 8 * u < Hkv * 16) v0[u] = __ldg(vs + kq + 8 * u);
     if (p0 < 0 || p0 > Tcap - Tq) {
       uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(tok) * Hq * 128);
       for (int i = kq; i < Hq * 16; i += 8) o[i] = zero4;
@@ -222,17 +283,18 @@ __global__ void __launch_bounds__(kPrologueThreads)
 #pragma unroll
     for (int i = 0; i < 8; ++i) rope_cos_sin(static_cast<float>(pos), tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
     const size_t row = static_cast<size_t>(b) * Tcap + pos;  // cache row of this token
-    rope_norm_token(q + static_cast<size_t>(tok) * Hq * 128, k_new + static_cast<size_t>(tok) * Hkv * 128,
-                    qn + static_cast<size_t>(tok) * Hq * 128, kcache + row * Hkv * 128, Hq, Hkv, kq, c, s, gmask,
-                    q_scale, 1.0f);
-    if (ve_new != nullptr) {  // the chunk's values with their gated embedding, into the cache
+    uint4* vd = reinterpret_cast<uint4*>(vcache + row * Hkv * 128);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (plain_v && kq + 8 * u < Hkv * 16) vd[kq + 8 * u] = v0[u];
+    rope_norm_token(qt, kt, qn + static_cast<size_t>(tok) * Hq * 128, kcache + row * Hkv * 128, Hq, Hkv, kq, c, s,
+                    gmask, q_scale, 1.0f, lo0, hi0);
+    if (!plain_v) {  // the chunk's values with their gated embedding, into the cache
       mix_values(v_new + static_cast<size_t>(tok) * Hkv * 128, ve_new + static_cast<size_t>(tok) * Hkv * 128,
                  ve_gate + static_cast<size_t>(tok) * Hkv, vcache + row * Hkv * 128, Hkv, kq);
       return;
     }
-    const uint4* vs = reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(tok) * Hkv * 128);
-    uint4* vd = reinterpret_cast<uint4*>(vcache + row * Hkv * 128);
-    for (int i = kq; i < Hkv * 16; i += 8) vd[i] = __ldg(vs + i);
+    if (Hkv * 16 > 32) copy_words(vd + 32, vs + 32, Hkv * 16 - 32, kq);  // words past the first four per lane
     return;
   }
   // V tail copy: row i of sequence b
@@ -244,16 +306,15 @@ __global__ void __launch_bounds__(kPrologueThreads)
   const int key = ((p0 + Tq - 1) / 128) * 128 + i;
   uint4* d = reinterpret_cast<uint4*>(vtail + (static_cast<size_t>(b) * 128 + i) * Hkv * 128);
   if (key < p0) {  // an earlier cache row (not written by this kernel)
-    const uint4* src = reinterpret_cast<const uint4*>(vcache + (static_cast<size_t>(b) * Tcap + key) * Hkv * 128);
-    for (int e = kq; e < Hkv * 16; e += 8) d[e] = src[e];
+    copy_words(d, reinterpret_cast<const uint4*>(vcache + (static_cast<size_t>(b) * Tcap + key) * Hkv * 128),
+               Hkv * 16, kq);
   } else if (key < p0 + Tq) {  // a row of the chunk (mixed with its value embedding, as the cache row is)
     const size_t tk = static_cast<size_t>(b) * Tq + (key - p0);
     if (ve_new != nullptr) {
       mix_values(v_new + tk * Hkv * 128, ve_new + tk * Hkv * 128, ve_gate + tk * Hkv,
                  vtail + (static_cast<size_t>(b) * 128 + i) * Hkv * 128, Hkv, kq);
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(v_new + tk * Hkv * 128);
-      for (int e = kq; e < Hkv * 16; e += 8) d[e] = __ldg(src + e);
+      copy_words(d, reinterpret_cast<const uint4*>(v_new + tk * Hkv * 128), Hkv * 16, kq);
     }
   } else {
     for (int e = kq; e < Hkv * 16; e += 8) d[e] = zero4;
