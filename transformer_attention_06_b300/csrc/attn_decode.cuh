@@ -266,6 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int C = gridDim.x, c = blockIdx.x;
   const bool has_new = p.k_new != nullptr;
   const unsigned long long lim = p.wait_limit_ns;
+  // Launched with programmatic dependent launch: the next kernel in the stream may be scheduled now (its CTAs take
+  // SMs as this grid's CTAs exit, and wait for this grid to complete before reading anything), and this grid's own
+  // set-up below runs while the previous kernel drains; nothing an earlier kernel may write (cache lengths, q, the
+  // caches, the workspace) is read before the griddepcontrol.wait further down.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ------------------------------------------------------------------ set-up: barriers, TMEM, operand padding
   if (tid == 0) {
@@ -301,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Q slots and P buffers start all-zero: rows >= G are never written again and must contribute nothing.
   for (int i = tid; i < (kQSlots + 2) * kOpBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
-  for (int b = tid; b < min(p.B, kLensCache); b += kThreads) lens_s[b] = __ldg(p.cache_lens + b);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int b = tid; b < min(p.B, kLensCache); b += kThreads) lens_s[b] = p.cache_lens[b];
   __syncthreads();
 
   // ------------------------------------------------------------------ set-up: N and this CTA's first tile

@@ -208,11 +208,24 @@ DecodeLayout decode_layout(int B, int Hq, int Hkv) {
   return L;
 }
 
+// The decode kernel is launched with programmatic dependent launch: its CTAs may start (barriers, TMEM, operand
+// padding) while the previous kernel in the stream drains, and wait for it (griddepcontrol.wait) before reading any
+// input.  A launch failure is left for the caller's cudaGetLastError check.
 template <int G>
 void launch_decode_g(int grid, const CUtensorMap& mk, const CUtensorMap& mv, const RopeTable& tab,
                      const nc::dec::Params& prm, cudaStream_t stream) {
   set_smem_attr_once(nc::dec::attn_decode_kernel<G>, nc::dec::kSmemBytes, G);
-  nc::dec::attn_decode_kernel<G><<<grid, nc::dec::kThreads, nc::dec::kSmemBytes, stream>>>(mk, mv, tab, prm);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(nc::dec::kThreads);
+  cfg.dynamicSmemBytes = nc::dec::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  (void)cudaLaunchKernelEx(&cfg, nc::dec::attn_decode_kernel<G>, mk, mv, tab, prm);
 }
 
 // Resident CTAs of the decode kernel on the current device: one per SM, at most kMaxParts.
