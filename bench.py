@@ -264,15 +264,15 @@ def oracle_fwd_sample(wl, W, batches, groups=None):
 
 
 def cpu_baseline():
-    """The oracle on the long-context workload: both batch rows of the W=1024 call and batch row 0 of the W=8192
-    call (about 300 in-band GFLOP)."""
+    """The oracle on one whole long-context step: the W=1024 and the W=8192 call on both batch rows (about 509
+    in-band GFLOP, some 10 s of host time)."""
     f1, t1 = oracle_fwd_sample(LONG, 1024, LONG.B)
-    f2, t2 = oracle_fwd_sample(LONG, 8192, 1)
+    f2, t2 = oracle_fwd_sample(LONG, 8192, LONG.B)
     flops, dt = f1 + f2, t1 + t2
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"long-context workload (B=2, T=8192, Hq=12, Hkv=4): the W=1024 call on both batch rows and "
-                      f"the W=8192 call on batch row 0, numpy fp64, {flops / 1e9:.1f} in-band GFLOP in {dt:.1f} s "
-                      f"on {cpu_model()} ({os.cpu_count()} logical cores)"}
+            "sample": f"one long-context step (B=2, T=8192, Hq=12, Hkv=4): the W=1024 and W=8192 calls on both batch "
+                      f"rows, numpy fp64, {flops / 1e9:.1f} in-band GFLOP in {dt:.1f} s on {cpu_model()} "
+                      f"({os.cpu_count()} logical cores)"}
 
 
 def run_reference(args, ws, rank):
@@ -609,7 +609,7 @@ def run_ours(args, ws, rank, local):
                           f"replayed from a CUDA graph after a 512 MiB L2 flush outside the events")}
         del kc, vc
 
-    # ---- backward pass (CUDA-core kernels) on the depth-12 layer shapes
+    # ---- backward pass (tcgen05 kernels) on the depth-12 layer shapes
     bwd = None
     if "backward" in sections:
         w = DEPTH12
@@ -634,11 +634,37 @@ def run_ours(args, ws, rank, local):
             tot_f += fl
             tot_us += us
         val = tot_f / (tot_us * 1e-6) / 1e12
+        # the training path: the forward keeps its output and row statistics, the backward reuses them
+        saved, s_f, s_us = {}, 0.0, 0.0
+        for W in sorted(set(w.windows)):
+            bo, blse = nc.nc_attn_fwd_lse(bq, bk, bv, window=W)
+            nc.nc_attn_bwd_saved(bq, bk, bv, bo, bdo, blse, window=W, workspace=bws)
+            torch.cuda.synchronize()
+            n_b = 10
+            evs = [(mk(), mk()) for _ in range(n_b)]
+            for i in range(n_b):
+                flush.fill_(i)
+                evs[i][0].record(stream)
+                nc.nc_attn_bwd_saved(bq, bk, bv, bo, bdo, blse, window=W, workspace=bws)
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+            us = dist_max(sum(a.elapsed_time(b) for a, b in evs) * 1e3 / n_b, ws)
+            fl = 2.5 * fwd_flops(w.B, w.T, w.Hq, w.D, W)
+            saved[str(W)] = {"us_per_call": us, "tflops": fl / (us * 1e-6) / 1e12}
+            s_f += fl
+            s_us += us
+            del bo, blse
         bwd = {"value": val, "unit": "TFLOP/s", "frac": val / peaks["bf16_tflops"], "windows": per_w,
                "config": (f"{w.name} layer shapes, windows {sorted(set(w.windows))}; one nc_attn_bwd_ws call: the forward "
                           f"recomputed for its row statistics, then dK/dV and dQ on tcgen05 and the norm/RoPE backward; "
                           f"dq, dk, dv in fp32; FLOPs counted as 3.5x the forward's in-band FLOPs (2 products of the "
-                          f"forward, 5 of the backward); L2 flushed before each call")}
+                          f"forward, 5 of the backward); L2 flushed before each call"),
+               "saved_statistics": {
+                   "value": s_f / (s_us * 1e-6) / 1e12, "unit": "TFLOP/s",
+                   "frac": s_f / (s_us * 1e-6) / 1e12 / peaks["bf16_tflops"], "windows": saved,
+                   "config": ("one nc_attn_bwd_saved_ws call on the output and log-sum-exp kept by nc_attn_fwd_lse "
+                              "(no forward recomputation; rowsum(dO O) from the kept output); FLOPs counted as 2.5x "
+                              "the forward's in-band FLOPs (the backward's 5 products); L2 flushed before each call")}}
         del bq, bk, bv, bdo, bws
 
     st = nc.nc_attn_get_device_status(clear=True)

@@ -227,6 +227,34 @@ nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void
                          float* dv, int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---- training: forward that keeps its row statistics, backward that reuses them ------------------------------
+ * A training step normally keeps the forward's output and the log-sum-exp of every score row for the backward, so
+ * that the backward does not run the forward again ("nanochat Admin & Developer Guide", section 3: the model trains
+ * through this block).
+ *
+ * nc_attn_fwd_lse_ws: nc_attn_fwd_ex plus `lse`, a device float buffer of nc_attn_lse_bytes(B, T, Hq, Hkv) bytes,
+ * 16-byte aligned, into which it writes the base-2 log-sum-exp log2(sum_j 2^s_j) of every query row's logits
+ * s_j = qk_gain log2(e) qn . kn_j / sqrt(D), in the layout the backward reads: float[B][Hkv][ceil(T / P)][128]
+ * with P = floor(128 / G), G = Hq / Hkv; entry r of block m of (b, kv head g) belongs to query position m P + r / G
+ * of query head g G + r % G, and entries that hold no query are 0.  Not with a value embedding or e4m3 operands.
+ *
+ * nc_attn_bwd_saved_ws: the gradients of nc_attn_bwd_ws from the same inputs plus that forward's `out` [B,T,Hq,D]
+ * (bf16) and `lse`; it skips the forward's recomputation and forms rowsum(dout * out) from the kept output.  Same
+ * workspace (nc_attn_bwd_workspace_bytes) and the same window, rope_base and qk_gain as the forward's.  Returns 0
+ * bytes / NC_ERR_INVALID_ARG for the shapes and pointers nc_attn_bwd_ws rejects, and for a null or misaligned
+ * out or lse.
+ */
+size_t nc_attn_lse_bytes(int B, int T, int Hq, int Hkv);
+
+nc_status nc_attn_fwd_lse_ws(const void* q, const void* k, const void* v, void* out, float* lse, int B, int T, int Hq,
+                             int Hkv, int D, int window, float rope_base, float qk_gain, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+nc_status nc_attn_bwd_saved_ws(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                               const float* lse, float* dq, float* dk, float* dv, int B, int T, int Hq, int Hkv,
+                               int D, int window, float rope_base, float qk_gain, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
 /* ---- KV-cache single-token decode ------------------------------------------------------------------------------
  * One new query token per sequence b, at position p_b = cache_lens[b].
  *   q:[B,Hq,D]            raw query of the new token (roped at position p_b, then normed, inside the call)

@@ -169,6 +169,35 @@ def test_bwd_rejects_bad_arguments(nc):
     assert call(Hq=256, Hkv=1) == U             # group larger than one 128-row tile
 
 
+def test_saved_statistics_entry_points_reject_bad_arguments(nc):
+    E, U, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_UNSUPPORTED, nc.NC_ERR_WORKSPACE
+    # statistics of B=4, T=2048, Hq=Hkv=6 (G = 1: P = 128 positions per tile, 16 tiles): one float per packed row
+    assert nc.lib.nc_attn_lse_bytes(4, 2048, 6, 6) == 4 * 6 * 16 * 128 * 4
+    # G = 3: P = 42 positions per tile, ceil(300 / 42) = 8 tiles per kv head, 128 rows each (126 hold queries)
+    assert nc.lib.nc_attn_lse_bytes(1, 300, 3, 1) == 8 * 128 * 4
+    assert nc.lib.nc_attn_lse_bytes(1, 300, 4, 3) == 0
+    fwd = nc.lib.nc_attn_fwd_lse_ws
+
+    def f(q=P, lse=P, B=1, T=64, Hq=4, Hkv=2, D=128, gain=1.0, ws=None, wsb=0):
+        return fwd(q, P, P, P, lse, B, T, Hq, Hkv, D, -1, 1e5, gain, ws, wsb, None)
+    assert f(lse=None) == E
+    assert f(lse=PM) == E                      # misaligned statistics buffer
+    assert f(q=None) == E
+    assert f(gain=5.0) == E
+    assert f(D=64) == U
+    assert f() == WS
+    bwd = nc.lib.nc_attn_bwd_saved_ws
+
+    def g(out=P, lse=P, B=1, T=64, Hq=4, Hkv=2, D=128, ws=None, wsb=0):
+        return bwd(P, P, P, out, P, lse, P, P, P, B, T, Hq, Hkv, D, -1, 1e5, 1.0, ws, wsb, None)
+    assert g(out=None) == E
+    assert g(lse=None) == E
+    assert g(out=PM) == E
+    assert g(Hq=3, Hkv=2) == E
+    assert g(D=64) == U
+    assert g() == WS
+
+
 def test_fwd_ve_rejects_bad_arguments(nc):
     E, WS = nc.NC_ERR_INVALID_ARG, nc.NC_ERR_WORKSPACE
     f = nc.lib.nc_attn_fwd_ve

@@ -9,8 +9,11 @@ _EXPORTS = (
     "NcAttnError",
     "nc_attn_decode",
     "nc_attn_decode_workspace_bytes",
+    "nc_attn_bwd",
+    "nc_attn_bwd_saved",
     "nc_attn_fwd",
     "nc_attn_fwd_fp8",
+    "nc_attn_fwd_lse",
     "nc_attn_fwd_workspace_bytes",
     "nc_attn_get_device_status",
     "nc_attn_qk_prologue",

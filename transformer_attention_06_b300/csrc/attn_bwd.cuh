@@ -113,6 +113,48 @@ __global__ void __launch_bounds__(kPostThreads)
                        dk + (static_cast<size_t>(tok) * Hkv + h) * 128, kq, c, s, gmask);
 }
 
+// ---- rowsum(dO * O) from a kept forward output ---------------------------------------------------------------------
+// For a backward that reuses the forward's output and log-sum-exp instead of recomputing them: the rowsum of dout *
+// out (both bf16) of every packed query row, in the layout the tcgen05 kernels read -- row r of Q tile m of (b, kv
+// head g) is position m P + r / G of query head g G + r % G, and rows that hold no query get 0.  One 8-lane group
+// per row, 16 elements per lane; memory-bound.
+constexpr int kDrowThreads = 256;
+__global__ void __launch_bounds__(kDrowThreads)
+    drow_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout, float* __restrict__ drow,
+                int T, int Hq, int Hkv, int G, int P, int n_qtiles, long long n_rows) {
+  const long long row = static_cast<long long>(blockIdx.x) * (kDrowThreads / 8) + (threadIdx.x >> 3);
+  const int kq = threadIdx.x & 7;
+  if (row >= n_rows) return;  // whole 8-lane groups leave together
+  const unsigned gmask = 0xFFu << ((threadIdx.x & 31) & ~7);
+  const int r = static_cast<int>(row & 127);
+  const long long tile_row = row >> 7;
+  const int m = static_cast<int>(tile_row % n_qtiles);
+  const long long bg = tile_row / n_qtiles;
+  const int g = static_cast<int>(bg % Hkv);
+  const long long b = bg / Hkv;
+  const int t = m * P + r / G;
+  float acc = 0.f;
+  if (r < G * P && t < T) {
+    const size_t off = ((static_cast<size_t>(b) * T + t) * Hq + g * G + r % G) * 128;
+    const uint4* o4 = reinterpret_cast<const uint4*>(out + off);
+    const uint4* d4 = reinterpret_cast<const uint4*>(dout + off);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint4 a = __ldg(o4 + kq + 8 * u), d = __ldg(d4 + kq + 8 * u);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(bf16_lo(aw[e]), bf16_lo(dw[e]), acc);
+        acc = fmaf(bf16_hi(aw[e]), bf16_hi(dw[e]), acc);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(gmask, acc, 1);
+  acc += __shfl_xor_sync(gmask, acc, 2);
+  acc += __shfl_xor_sync(gmask, acc, 4);
+  if (kq == 0) drow[row] = acc;
+}
+
 // ---- tcgen05 kernels ---------------------------------------------------------------------------------------------
 constexpr int kThreads = 384;
 constexpr int kStages = 2;

@@ -334,8 +334,10 @@ static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out
                           int D, int window, float rope_base, float qk_gain, void* workspace,
                           size_t workspace_bytes, cudaEvent_t k1_begin, cudaEvent_t k2_begin, cudaEvent_t k2_end,
                           cudaStream_t stream, const void* ve = nullptr, const void* ve_gate = nullptr,
-                          bool fp8 = false) {
+                          bool fp8 = false, float* lse_out = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return NC_ERR_INVALID_ARG;
+  if (lse_out != nullptr && (fp8 || ve != nullptr || (reinterpret_cast<uintptr_t>(lse_out) & 15u) != 0))
+    return NC_ERR_INVALID_ARG;
   if (!(qk_gain > 0.f && qk_gain <= kMaxQkGain)) return NC_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return NC_ERR_INVALID_ARG;
   if (window < -1 || !rope_base_ok(rope_base)) return NC_ERR_INVALID_ARG;
@@ -398,7 +400,7 @@ static nc_status fwd_impl(const void* q, const void* k, const void* v, void* out
   prm.Tk = T;
   prm.window = window;
   prm.wait_limit_ns = kWaitLimitNs;
-  prm.lse = nullptr;
+  prm.lse = lse_out;  // with it: every query row's base-2 log-sum-exp, for a backward that reuses it
   prm.drow = nullptr;
   prm.dout = nullptr;
   prm.n_qtiles = (T + P - 1) / P;
@@ -465,6 +467,14 @@ nc_status nc_attn_fwd_ex(const void* q, const void* k, const void* v, void* out,
                          cudaStream_t stream) {
   return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace, workspace_bytes, nullptr,
                   nullptr, nullptr, stream);
+}
+
+nc_status nc_attn_fwd_lse_ws(const void* q, const void* k, const void* v, void* out, float* lse, int B, int T, int Hq,
+                             int Hkv, int D, int window, float rope_base, float qk_gain, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  if (lse == nullptr) return NC_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, out, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace, workspace_bytes, nullptr,
+                  nullptr, nullptr, stream, nullptr, nullptr, false, lse);
 }
 
 nc_status nc_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int T, int Hq, int Hkv, int D,
@@ -627,11 +637,23 @@ size_t nc_attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
   return bwd_layout(B, T, Hq, Hkv).total;
 }
 
-nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void* dout, float* dq, float* dk,
-                         float* dv, int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+size_t nc_attn_lse_bytes(int B, int T, int Hq, int Hkv) {
+  if (check_fwd_shapes(B, T, Hq, Hkv, 128) != NC_OK || Hq / Hkv > 128) return 0;
+  const BwdLayout L = bwd_layout(B, T, Hq, Hkv);
+  return L.drow - L.lse;  // the row-statistics block of the backward workspace: rows * 4 bytes, rounded up
+}
+
+// The backward of nc_attn_bwd_ws; with `out` and `lse_in` (the forward's output and its nc_attn_fwd_lse_ws
+// statistics) the forward is not run again: rowsum(dout * out) comes from the kept output.
+static nc_status bwd_impl(const void* q, const void* k, const void* v, const void* dout, float* dq, float* dk,
+                          float* dv, int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream, const void* out = nullptr,
+                          const float* lse_in = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||
       dv == nullptr)
+    return NC_ERR_INVALID_ARG;
+  if ((out == nullptr) != (lse_in == nullptr)) return NC_ERR_INVALID_ARG;
+  if (out != nullptr && (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse_in) & 15u) != 0))
     return NC_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
       !aligned16(dv))
@@ -665,7 +687,19 @@ nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void
   const RopeTable tab = rope_table(rope_base);
   st = launch_prologue(q, k, qn, kn, B, T, Hq, Hkv, tab, scale_log2_for_d128() * qk_gain, ctr, stream);
   if (st != NC_OK) return st;
-  // 2. the forward's row statistics (no output written: the output map points at qn', which has its shape)
+  // 2. the forward's row statistics: kept from the forward (rowsum(dout * out) from its output), or recomputed by
+  // the attention kernel in its statistics mode (no output written: the output map points at qn', which has its
+  // shape)
+  if (lse_in != nullptr) {
+    lse = const_cast<float*>(lse_in);
+    const long long n_rows = static_cast<long long>(B) * Hkv * L.n_qtiles * 128;
+    const long long blocks = (n_rows + nc::bwd::kDrowThreads / 8 - 1) / (nc::bwd::kDrowThreads / 8);
+    nc::bwd::drow_kernel<<<static_cast<unsigned>(blocks), nc::bwd::kDrowThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), drow, T, Hq, Hkv, G, P,
+        L.n_qtiles, n_rows);
+    st = launch_status();
+    if (st != NC_OK) return st;
+  }
   int n_pairs = 0, tpi = 0, G2 = 0, P2 = 0;
   if (!fwd_split(B, T, Hq, Hkv, n_sm, G2, P2, n_pairs, tpi)) return NC_ERR_UNSUPPORTED;
   nc::fwd::Params fp;
@@ -689,8 +723,10 @@ nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void
   fp.dout = static_cast<const __nv_bfloat16*>(dout);
   fp.n_qtiles = L.n_qtiles;
   fp.store_out = 0;
-  st = launch_attention(mq, mk, mv, mv, mq, fp, n_sm, stream);
-  if (st != NC_OK) return st;
+  if (lse_in == nullptr) {
+    st = launch_attention(mq, mk, mv, mv, mq, fp, n_sm, stream);
+    if (st != NC_OK) return st;
+  }
   // 3. dK (w.r.t. kn) and dV;  4. dQ (w.r.t. qn)
   nc::bwd::Params bp;
   bp.lse = lse;
@@ -725,6 +761,22 @@ nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void
   nc::bwd::bwd_norm_rope_kernel<<<blocks, nc::bwd::kPostThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), dq, dk, BT, T, Hq, Hkv, tab);
   return launch_status();
+}
+
+nc_status nc_attn_bwd_ws(const void* q, const void* k, const void* v, const void* dout, float* dq, float* dk,
+                         float* dv, int B, int T, int Hq, int Hkv, int D, int window, float rope_base, float qk_gain,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(q, k, v, dout, dq, dk, dv, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace,
+                  workspace_bytes, stream);
+}
+
+nc_status nc_attn_bwd_saved_ws(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                               const float* lse, float* dq, float* dk, float* dv, int B, int T, int Hq, int Hkv,
+                               int D, int window, float rope_base, float qk_gain, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  if (out == nullptr || lse == nullptr) return NC_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, dout, dq, dk, dv, B, T, Hq, Hkv, D, window, rope_base, qk_gain, workspace,
+                  workspace_bytes, stream, out, lse);
 }
 
 size_t nc_attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int Tcap, int window) {

@@ -49,6 +49,9 @@ def _load():
         "nc_attn_fwd_ve_workspace_bytes": (sz, [i, i, i, i, i]),
         "nc_attn_fwd_ve": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_bwd_ws": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
+        "nc_attn_lse_bytes": (sz, [i, i, i, i]),
+        "nc_attn_fwd_lse_ws": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
+        "nc_attn_bwd_saved_ws": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_prefill_chunk_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_decode_ex": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, vp, sz, vp]),
         "nc_attn_prefill_chunk_workspace_bytes": (sz, [i, i, i, i, i]),
@@ -269,6 +272,60 @@ def nc_attn_bwd(q, k, v, dout, window=-1, rope_base=ROPE_BASE, qk_gain=1.0, work
                             int(window), float(rope_base), float(qk_gain), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nc_attn_bwd")
+    return dq, dk, dv
+
+
+def nc_attn_fwd_lse(q, k, v, out=None, lse=None, window=-1, rope_base=ROPE_BASE, qk_gain=1.0, workspace=None,
+                    stream=None):
+    """Training forward: (out, lse) where lse holds every query row's base-2 log-sum-exp (float32, the packed layout
+    of nc_attn_lse_bytes / nc_attn_fwd_lse_ws: [B][Hkv][ceil(T / P)][128], P = 128 // (Hq // Hkv)) for
+    nc_attn_bwd_saved."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, name, 4)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if tuple(k.shape) != (B, T, Hkv, D) or tuple(v.shape) != (B, T, Hkv, D):
+        raise ValueError("k / v shapes do not match q")
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", 4)
+    nl = int(lib.nc_attn_lse_bytes(B, T, Hq, Hkv))
+    if lse is None:
+        lse = torch.empty(max(nl, 4) // 4, dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or not lse.is_cuda or lse.numel() * 4 < nl:
+        raise ValueError(f"lse must be a CUDA float32 tensor of at least {nl} bytes")
+    nbytes = int(lib.nc_attn_fwd_workspace_bytes(B, T, Hq, Hkv, D))
+    if workspace is None:
+        workspace = _workspace("fwd", nbytes, q.device, zero=False)
+    st = lib.nc_attn_fwd_lse_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, T, Hq, Hkv, D, int(window),
+                                float(rope_base), float(qk_gain), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nc_attn_fwd_lse")
+    return out, lse
+
+
+def nc_attn_bwd_saved(q, k, v, out, dout, lse, window=-1, rope_base=ROPE_BASE, qk_gain=1.0, workspace=None,
+                      stream=None):
+    """Gradients (dq, dk, dv) like nc_attn_bwd, reusing the output and lse of nc_attn_fwd_lse instead of running the
+    forward again."""
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, name, 4)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if (tuple(k.shape) != (B, T, Hkv, D) or tuple(v.shape) != (B, T, Hkv, D) or tuple(dout.shape) != tuple(q.shape)
+            or tuple(out.shape) != tuple(q.shape)):
+        raise ValueError("k / v / out / dout shapes do not match q")
+    if lse.dtype != torch.float32 or not lse.is_cuda or lse.numel() * 4 < int(lib.nc_attn_lse_bytes(B, T, Hq, Hkv)):
+        raise ValueError("lse must be the float32 statistics of nc_attn_fwd_lse for these shapes")
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    nbytes = int(lib.nc_attn_bwd_workspace_bytes(B, T, Hq, Hkv, D))
+    if workspace is None:
+        workspace = _workspace("bwd", nbytes, q.device, zero=False)
+    st = lib.nc_attn_bwd_saved_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), B, T, Hq, Hkv, D, int(window), float(rope_base), float(qk_gain),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nc_attn_bwd_saved")
     return dq, dk, dv
 
 
