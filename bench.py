@@ -445,7 +445,8 @@ def run_ours(args, ws, rank, local):
         dev_sets = [[(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o), W)
                      for (q, k, v, o, W) in layers] for _ in range(2)]
         s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        n_e2e = max(3, min(args.steps, 10))
+        # enough steps that the pipeline's fill (the first inputs) and drain (the last outputs) are a small share
+        n_e2e = min(max(20, args.steps), 40)
         n_warm = 2
         ev = lambda: torch.cuda.Event()  # noqa: E731
         h2d_done = [[ev() for _ in layers] for _ in range(2)]

@@ -81,6 +81,20 @@ def test_fwd_odd_shapes(nc, B, T, Hq, Hkv, W):
     assert_close(out, ref.attn_fwd(f64(q), f64(k), f64(v), W), f"B{B} T{T} Hq{Hq} Hkv{Hkv} W{W}")
 
 
+# Single-tile items (too few pairs to give every SM an item) run their key tiles as two chains whose partial sums the
+# epilogue adds.  With G = 1 (128 positions per Q tile) and one sequence, Q tile m of a T = 640 layer has m + 1 key
+# tiles under a causal mask: 1 to 5 rounds, i.e. chain B empty, one tile each, A one tile longer than B; the windows put
+# a band edge in the first chain's tiles, in the second's, or in both.
+SPLIT = [(1, 640, 1, 1, W) for W in (-1, 0, 100, 200, 300, 511)] + [(1, 600, 2, 2, 250), (1, 1000, 3, 3, -1)]
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,W", SPLIT)
+def test_fwd_split_items(nc, B, T, Hq, Hkv, W):
+    q, k, v = fwd_inputs(B, T, Hq, Hkv, 128, seed=3 * T + W)
+    out = nc.nc_attn_fwd(*cuda(q, k, v), window=W)
+    assert_close(out, ref.attn_fwd(f64(q), f64(k), f64(v), W), f"split items B{B} T{T} Hq{Hq} Hkv{Hkv} W{W}")
+
+
 def assert_close_rows(got, exp, what):
     """Element-wise comparison of a whole [B, T, H, D] output; names the worst (b, t, h) row on failure."""
     g = f64(got)
