@@ -3,6 +3,7 @@
 // a single symbol without relocatable device code.
 //
 // Nothing here falls back to the CPU or to another implementation: an unsupported request returns an error code.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -117,24 +118,39 @@ void set_smem_attr_once(F* kernel, int bytes, int slot) {
 
 nc_status launch_status() { return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA; }
 
+int sm_count();
+
+// Slices per token for the prologue kernels: as many as keep the grid within one wave of lane groups (64 resident
+// groups per SM: two blocks of 256 threads at 128 registers), so short inputs spread over every SM (a chunk of 2048
+// tokens: 4 slices) while a partial second wave never appears (8192 tokens: 1 slice), at most kMaxSlices and at most
+// one per q/k head.
+int prologue_slices(long long tokens, int H) {
+  const long long wave = static_cast<long long>(std::max(sm_count(), 1)) * 64;
+  const long long s = wave / std::max(tokens, 1LL);
+  return static_cast<int>(std::max(1LL, std::min<long long>({s, nc::kMaxSlices, H})));
+}
+
 // fp8: qn, kn written as e4m3 codes times q_scale, k_scale (else bf16, kn unscaled).
 nc_status launch_prologue(const void* q, const void* k, void* qn, void* kn, int B, int T, int Hq, int Hkv,
                           const RopeTable& tab, float q_scale, unsigned* zero_word, cudaStream_t stream,
                           const void* v = nullptr, const void* ve = nullptr, const void* ve_gate = nullptr,
                           void* vmix = nullptr, bool fp8 = false, float k_scale = 1.0f) {
   const int BT = B * T;
-  const int blocks = (BT + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
+  const int ns = prologue_slices(BT, Hq + Hkv);
+  const long long groups = static_cast<long long>(BT) * ns;
+  if (groups > 0x7fffffffLL - nc::kPrologueTokensPerBlock) return NC_ERR_UNSUPPORTED;
+  const int blocks = static_cast<int>((groups + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock);
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* kb = static_cast<const __nv_bfloat16*>(k);
   if (fp8) {
     nc::qk_prologue_kernel<uint8_t><<<blocks, nc::kPrologueThreads, 0, stream>>>(
         qb, kb, static_cast<uint8_t*>(qn), static_cast<uint8_t*>(kn), BT, T, Hq, Hkv, tab, q_scale, k_scale,
-        zero_word, nullptr, nullptr, nullptr, nullptr);
+        zero_word, nullptr, nullptr, nullptr, nullptr, ns);
   } else {
     nc::qk_prologue_kernel<__nv_bfloat16><<<blocks, nc::kPrologueThreads, 0, stream>>>(
         qb, kb, static_cast<__nv_bfloat16*>(qn), static_cast<__nv_bfloat16*>(kn), BT, T, Hq, Hkv, tab, q_scale,
         k_scale, zero_word, static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(ve),
-        static_cast<const __nv_bfloat16*>(ve_gate), static_cast<__nv_bfloat16*>(vmix));
+        static_cast<const __nv_bfloat16*>(ve_gate), static_cast<__nv_bfloat16*>(vmix), ns);
   }
   return launch_status();
 }
@@ -536,14 +552,17 @@ static nc_status chunk_impl(const void* q, const void* k_new, const void* v_new,
       !make_map_4d(&mo, out, 128, Hq, Tq, B, 64, G, P, 1))
     return NC_ERR_CUDA;
 
-  const int tok_blocks = (B * Tq + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
+  const int ns = prologue_slices(static_cast<long long>(B) * Tq, Hq + Hkv);
+  const long long groups = static_cast<long long>(B) * Tq * ns;
+  if (groups > 0x7fffffffLL - nc::kPrologueTokensPerBlock) return NC_ERR_UNSUPPORTED;
+  const int tok_blocks = static_cast<int>((groups + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock);
   const int tail_blocks = (B * 128 + nc::kPrologueTokensPerBlock - 1) / nc::kPrologueTokensPerBlock;
   nc::chunk_prologue_kernel<<<tok_blocks + tail_blocks, nc::kPrologueThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
       static_cast<const __nv_bfloat16*>(v_new), static_cast<__nv_bfloat16*>(qn), static_cast<__nv_bfloat16*>(kcache),
       static_cast<__nv_bfloat16*>(vcache), static_cast<__nv_bfloat16*>(vtail), static_cast<__nv_bfloat16*>(out),
       cache_lens, B, Tq, Hq, Hkv, Tcap, tok_blocks, rope_table(rope_base), scale_log2_for_d128() * qk_gain,
-      item_ctr, static_cast<const __nv_bfloat16*>(ve_new), static_cast<const __nv_bfloat16*>(ve_gate));
+      item_ctr, static_cast<const __nv_bfloat16*>(ve_new), static_cast<const __nv_bfloat16*>(ve_gate), ns);
   st = launch_status();
   if (st != NC_OK) return st;
 

@@ -75,35 +75,36 @@ __device__ __forceinline__ void store_head(void* dst, int kq, const float (&y1)[
   }
 }
 
-// The first round of rope_norm_token: slices kq and kq + 8 of heads 0..3 of the token's list of Hq q heads followed
-// by its Hkv k heads.  It depends on nothing but the token, so callers issue it before computing the position's
-// cos / sin (and, in the chunked prefill, before the cache length has arrived).
+// The first round of rope_norm_token: slices kq and kq + 8 of heads i0 .. i0 + 3 (those below i1) of the token's
+// list of Hq q heads followed by its Hkv k heads.  It depends on nothing but the token, so callers issue it before
+// computing the position's cos / sin (and, in the chunked prefill, before the cache length has arrived).
 __device__ __forceinline__ void load_first_heads(const __nv_bfloat16* __restrict__ q,
-                                                 const __nv_bfloat16* __restrict__ k, int Hq, int Hkv, int kq,
+                                                 const __nv_bfloat16* __restrict__ k, int Hq, int i0, int i1, int kq,
                                                  uint4 (&lo)[4], uint4 (&hi)[4]) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    if (u < Hq + Hkv) {
-      const uint4* p = reinterpret_cast<const uint4*>(u < Hq ? q + u * 128 : k + (u - Hq) * 128);
+    const int i = i0 + u;
+    if (i < i1) {
+      const uint4* p = reinterpret_cast<const uint4*>(i < Hq ? q + i * 128 : k + (i - Hq) * 128);
       lo[u] = __ldg(p + kq);
       hi[u] = __ldg(p + 8 + kq);
     }
   }
 }
 
-// The Hq q heads then the Hkv k heads of one token (q, k, qn, kn point at the token's head 0), in rounds of four
-// heads whose loads are issued one round ahead: while a round is rotated, normalised and stored, the next round's
-// sixteen 16-byte loads per lane are in flight.  (lo0, hi0) hold the first round, from load_first_heads.  OutT =
-// __nv_bfloat16 writes bf16 rows of 256 bytes; OutT = uint8_t writes e4m3 rows of 128 bytes (the values times the
-// scale, rounded to nearest even).
+// Heads [i0, i1) of one token's list of its Hq q heads followed by its Hkv k heads (q, k, qn, kn point at the
+// token's head 0), in rounds of four heads whose loads are issued one round ahead: while a round is rotated,
+// normalised and stored, the next round's sixteen 16-byte loads per lane are in flight.  (lo0, hi0) hold the first
+// round, from load_first_heads.  OutT = __nv_bfloat16 writes bf16 rows of 256 bytes; OutT = uint8_t writes e4m3 rows
+// of 128 bytes (the values times the scale, rounded to nearest even).
 template <typename OutT>
 __device__ __forceinline__ void rope_norm_token(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                                                OutT* __restrict__ qn, OutT* __restrict__ kn, int Hq, int Hkv, int kq,
-                                                const float (&c)[8], const float (&s)[8], unsigned gmask,
+                                                OutT* __restrict__ qn, OutT* __restrict__ kn, int Hq, int i0, int i1,
+                                                int kq, const float (&c)[8], const float (&s)[8], unsigned gmask,
                                                 float q_scale, float k_scale, const uint4 (&lo0)[4],
                                                 const uint4 (&hi0)[4]) {
   constexpr bool kE4m3 = sizeof(OutT) == 1;
-  const int H = Hq + Hkv;
+  const int H = i1;
   auto src = [&](int i) {
     return reinterpret_cast<const uint4*>(i < Hq ? q + i * 128 : k + (i - Hq) * 128);
   };
@@ -113,7 +114,7 @@ __device__ __forceinline__ void rope_norm_token(const __nv_bfloat16* __restrict_
     lo[0][u] = lo0[u];
     hi[0][u] = hi0[u];
   }
-  for (int h0 = 0; h0 < H; h0 += 8) {
+  for (int h0 = i0; h0 < H; h0 += 8) {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int base = h0 + 4 * half;
@@ -197,7 +198,24 @@ __device__ __forceinline__ void copy_words(uint4* dst, const uint4* src, int n, 
 }
 
 constexpr int kPrologueThreads = 256;
-constexpr int kPrologueTokensPerBlock = kPrologueThreads / 8;
+constexpr int kPrologueTokensPerBlock = kPrologueThreads / 8;  // 8-lane groups per block
+constexpr int kMaxSlices = 4;
+
+// A token's work split over n_slices 8-lane groups, so that short inputs still give every SM enough groups: slice sl
+// takes heads [H sl / n, H (sl + 1) / n) of its H = Hq + Hkv q and k heads and the same share of its Hkv value heads.
+struct Slice {
+  int tok, i0, i1, v0, v1;
+};
+__device__ __forceinline__ Slice slice_of(int gid, int n_slices, int Hq, int Hkv) {
+  Slice r;
+  r.tok = gid / n_slices;
+  const int sl = gid - r.tok * n_slices, H = Hq + Hkv;
+  r.i0 = H * sl / n_slices;
+  r.i1 = H * (sl + 1) / n_slices;
+  r.v0 = Hkv * sl / n_slices;
+  r.v1 = Hkv * (sl + 1) / n_slices;
+  return r;
+}
 
 // OutT: __nv_bfloat16 (qn, kn in bf16) or uint8_t (qn, kn in e4m3, scaled by q_scale and k_scale).
 template <typename OutT>
@@ -206,29 +224,31 @@ __global__ void __launch_bounds__(kPrologueThreads)
                        OutT* __restrict__ qn, OutT* __restrict__ kn, int BT, int T, int Hq,
                        int Hkv, const __grid_constant__ RopeTable tab, float q_scale, float k_scale, unsigned* zero_word,
                        const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ ve,
-                       const __nv_bfloat16* __restrict__ ve_gate, __nv_bfloat16* __restrict__ vmix) {
+                       const __nv_bfloat16* __restrict__ ve_gate, __nv_bfloat16* __restrict__ vmix, int n_slices) {
   // The attention kernel that follows in stream order may be scheduled now; it waits for this grid to complete
   // before reading anything written here.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // The attention kernel takes its work items from this counter.
   if (zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0u;
-  const int tok = blockIdx.x * kPrologueTokensPerBlock + (threadIdx.x >> 3);
+  const Slice w = slice_of(blockIdx.x * kPrologueTokensPerBlock + (threadIdx.x >> 3), n_slices, Hq, Hkv);
+  const int tok = w.tok;
   const int kq = threadIdx.x & 7;
   if (tok >= BT) return;  // whole 8-lane groups leave together
   const unsigned gmask = 0xFFu << ((threadIdx.x & 31) & ~7);
   const __nv_bfloat16* qt = q + static_cast<size_t>(tok) * Hq * 128;
   const __nv_bfloat16* kt = k + static_cast<size_t>(tok) * Hkv * 128;
   uint4 lo0[4], hi0[4];
-  load_first_heads(qt, kt, Hq, Hkv, kq, lo0, hi0);
+  load_first_heads(qt, kt, Hq, w.i0, w.i1, kq, lo0, hi0);
   const float pos = static_cast<float>(tok % T);
   float c[8], s[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) rope_cos_sin(pos, tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
   rope_norm_token(qt, kt, qn + static_cast<size_t>(tok) * Hq * 128, kn + static_cast<size_t>(tok) * Hkv * 128, Hq,
-                  Hkv, kq, c, s, gmask, q_scale, k_scale, lo0, hi0);
-  if (ve != nullptr)
-    mix_values(v + static_cast<size_t>(tok) * Hkv * 128, ve + static_cast<size_t>(tok) * Hkv * 128,
-               ve_gate + static_cast<size_t>(tok) * Hkv, vmix + static_cast<size_t>(tok) * Hkv * 128, Hkv, kq);
+                  w.i0, w.i1, kq, c, s, gmask, q_scale, k_scale, lo0, hi0);
+  if (ve != nullptr) {
+    const size_t o = static_cast<size_t>(tok) * Hkv + w.v0;
+    mix_values(v + o * 128, ve + o * 128, ve_gate + o, vmix + o * 128, w.v1 - w.v0, kq);
+  }
 }
 
 // Chunked prefill against a KV cache ("nanochat Admin & Developer Guide", section 6, SDPA case 3 "chunked /
@@ -241,7 +261,7 @@ __global__ void __launch_bounds__(kPrologueThreads)
 //     probability by whatever the cache holds beyond its valid rows;
 //   * a sequence whose p0 is outside [0, Tcap - Tq] gets a zero output, its cache is left alone and the device
 //     status records NC_DEV_BAD_CACHE_LEN.
-// Blocks [0, n_tok_blocks) take one token per 8-lane group, the rest one row of a V tail copy per group.
+// Blocks [0, n_tok_blocks) take one slice of a token per 8-lane group, the rest one row of a V tail copy per group.
 __global__ void __launch_bounds__(kPrologueThreads)
     chunk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
                           const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ qn,
@@ -249,29 +269,33 @@ __global__ void __launch_bounds__(kPrologueThreads)
                           __nv_bfloat16* __restrict__ out, const int* __restrict__ cache_lens, int B, int Tq, int Hq,
                           int Hkv, int Tcap, int n_tok_blocks, const __grid_constant__ RopeTable tab, float q_scale,
                           unsigned* zero_word, const __nv_bfloat16* __restrict__ ve_new,
-                          const __nv_bfloat16* __restrict__ ve_gate) {
+                          const __nv_bfloat16* __restrict__ ve_gate, int n_slices) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0u;
   const int grp = threadIdx.x >> 3;
   const int kq = threadIdx.x & 7;
   const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
   if (static_cast<int>(blockIdx.x) < n_tok_blocks) {
-    const int tok = blockIdx.x * kPrologueTokensPerBlock + grp;
+    const Slice w = slice_of(blockIdx.x * kPrologueTokensPerBlock + grp, n_slices, Hq, Hkv);
+    const int tok = w.tok;
     if (tok >= B * Tq) return;  // whole 8-lane groups leave together
     const int b = tok / Tq, t = tok - b * Tq;
     // Everything read from the chunk is independent of the cache length: the first round of q / k heads and the
-    // first value words are requested together with it.
+    // first value words of this slice are requested together with it.
     const __nv_bfloat16* qt = q + static_cast<size_t>(tok) * Hq * 128;
     const __nv_bfloat16* kt = k_new + static_cast<size_t>(tok) * Hkv * 128;
-    const uint4* vs = reinterpret_cast<const uint4*>(v_new + static_cast<size_t>(tok) * Hkv * 128);
+    const size_t vo = static_cast<size_t>(tok) * Hkv + w.v0;  // this slice's value heads
+    const int vw = (w.v1 - w.v0) * 16;                        // and their 16-byte words
+    const uint4* vs = reinterpret_cast<const uint4*>(v_new + vo * 128);
     const int p0 = __ldg(cache_lens + b);
     uint4 lo0[4], hi0[4], v0[4];
-    load_first_heads(qt, kt, Hq, Hkv, kq, lo0, hi0);
+    load_first_heads(qt, kt, Hq, w.i0, w.i1, kq, lo0, hi0);
     const bool plain_v = ve_new == nullptr;
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (plain_v && kq + 8 * u < Hkv * 16) v0[u] = __ldg(vs + kq + 8 * u);
+      if (plain_v && kq + 8 * u < vw) v0[u] = __ldg(vs + kq + 8 * u);
     if (p0 < 0 || p0 > Tcap - Tq) {
+      if (w.i0 > 0) return;  // the token's first slice writes its zero output row
       uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(tok) * Hq * 128);
       for (int i = kq; i < Hq * 16; i += 8) o[i] = zero4;
       if (t == 0 && kq == 0) raise_status(NC_DEV_BAD_CACHE_LEN);
@@ -283,18 +307,18 @@ __global__ void __launch_bounds__(kPrologueThreads)
 #pragma unroll
     for (int i = 0; i < 8; ++i) rope_cos_sin(static_cast<float>(pos), tab.hi[kq * 8 + i], tab.lo[kq * 8 + i], c[i], s[i]);
     const size_t row = static_cast<size_t>(b) * Tcap + pos;  // cache row of this token
-    uint4* vd = reinterpret_cast<uint4*>(vcache + row * Hkv * 128);
+    uint4* vd = reinterpret_cast<uint4*>(vcache + (row * Hkv + w.v0) * 128);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (plain_v && kq + 8 * u < Hkv * 16) vd[kq + 8 * u] = v0[u];
-    rope_norm_token(qt, kt, qn + static_cast<size_t>(tok) * Hq * 128, kcache + row * Hkv * 128, Hq, Hkv, kq, c, s,
-                    gmask, q_scale, 1.0f, lo0, hi0);
+      if (plain_v && kq + 8 * u < vw) vd[kq + 8 * u] = v0[u];
+    rope_norm_token(qt, kt, qn + static_cast<size_t>(tok) * Hq * 128, kcache + row * Hkv * 128, Hq, w.i0, w.i1, kq,
+                    c, s, gmask, q_scale, 1.0f, lo0, hi0);
     if (!plain_v) {  // the chunk's values with their gated embedding, into the cache
-      mix_values(v_new + static_cast<size_t>(tok) * Hkv * 128, ve_new + static_cast<size_t>(tok) * Hkv * 128,
-                 ve_gate + static_cast<size_t>(tok) * Hkv, vcache + row * Hkv * 128, Hkv, kq);
+      mix_values(v_new + vo * 128, ve_new + vo * 128, ve_gate + vo, vcache + (row * Hkv + w.v0) * 128, w.v1 - w.v0,
+                 kq);
       return;
     }
-    if (Hkv * 16 > 32) copy_words(vd + 32, vs + 32, Hkv * 16 - 32, kq);  // words past the first four per lane
+    if (vw > 32) copy_words(vd + 32, vs + 32, vw - 32, kq);  // words past the first four per lane
     return;
   }
   // V tail copy: row i of sequence b
