@@ -713,6 +713,7 @@ static nc_status bwd_impl(const void* q, const void* k, const void* v, const voi
     lse = const_cast<float*>(lse_in);
     const long long n_rows = static_cast<long long>(B) * Hkv * L.n_qtiles * 128;
     const long long blocks = (n_rows + nc::bwd::kDrowThreads / 8 - 1) / (nc::bwd::kDrowThreads / 8);
+    if (blocks > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;  // one-dimensional grid
     nc::bwd::drow_kernel<<<static_cast<unsigned>(blocks), nc::bwd::kDrowThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), drow, T, Hq, Hkv, G, P,
         L.n_qtiles, n_rows);
