@@ -684,6 +684,8 @@ static nc_status bwd_impl(const void* q, const void* k, const void* v, const voi
   if (Hq / Hkv > 128) return NC_ERR_UNSUPPORTED;
   const BwdLayout L = bwd_layout(B, T, Hq, Hkv);
   if (static_cast<long long>(B) * Hkv * L.n_qtiles > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
+  // the rowsum kernel's one-dimensional grid: 32 packed rows per block
+  if (lse_in != nullptr && static_cast<long long>(B) * Hkv * L.n_qtiles * 4 > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < L.total || !aligned16(workspace)) return NC_ERR_WORKSPACE;
   const int n_sm = sm_count();
   if (n_sm < 1) return NC_ERR_CUDA;
@@ -713,7 +715,6 @@ static nc_status bwd_impl(const void* q, const void* k, const void* v, const voi
     lse = const_cast<float*>(lse_in);
     const long long n_rows = static_cast<long long>(B) * Hkv * L.n_qtiles * 128;
     const long long blocks = (n_rows + nc::bwd::kDrowThreads / 8 - 1) / (nc::bwd::kDrowThreads / 8);
-    if (blocks > 0x7fffffffLL) return NC_ERR_UNSUPPORTED;  // one-dimensional grid
     nc::bwd::drow_kernel<<<static_cast<unsigned>(blocks), nc::bwd::kDrowThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), drow, T, Hq, Hkv, G, P,
         L.n_qtiles, n_rows);
