@@ -46,6 +46,24 @@ def test_prologue_matches_oracle_and_has_unit_rms(nc):
         assert np.max(np.abs(rms - 1.0)) < 2.0 ** -8
 
 
+def test_prologue_rotation_is_accurate_at_large_positions(nc):
+    """Positions up to 2^16 - 1 (angles up to 6.6e4 rad on the fastest pair): every element of qn and kn lies within
+    one bf16 ulp of the exact fp64 value, plus 2^-17 for the values near zero, where the absolute error of the
+    rotation (below 1e-6) can exceed an ulp.  A wrong angle reduction at large positions shows up as errors ~1e-2."""
+    T = 1 << 16
+    q, k, _ = fwd_inputs(1, T, 2, 1, 128, seed=7)
+    qn, kn = nc.nc_attn_qk_prologue(*cuda(q, k))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([np.arange(64), np.arange(T - 2048, T), rng.integers(0, T, 2048)]))
+    for got, x in ((qn, q), (kn, k)):
+        r = ref.qk_prologue(f64(x)[:, rows], rows[None, :])
+        g = f64(got)[:, rows]
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126))) - 7)
+        err = np.abs(g - r) - ulp
+        assert err.max() <= 2.0 ** -17, f"worst excess over one ulp {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
+
+
 # ------------------------------------------------------------------------------------------------ prefill
 
 @pytest.mark.parametrize("W", TINY.windows)

@@ -418,16 +418,44 @@ struct RopeTable {
 
 constexpr float kRmsEps = 1e-6f;
 
-// cos / sin of the angle pos * theta with an fp32-pair angle: the fp32 product, its exact rounding error (fma)
-// and the contribution of the residual of theta are summed into a small correction `d`, applied to first order
-// around sincosf of the rounded angle.  Accurate to ~1e-7 for pos < 2^24.
+// cos / sin of the angle pos * theta, theta given as an fp32 pair (th_hi + th_lo).  The angle is pos * th_hi rounded
+// to fp32 plus a small correction d (that product's exact rounding error, from an fma, and pos * th_lo).  It is
+// reduced by quarter turns with the Cody-Waite method (W. J. Cody and W. Waite, "Software Manual for the Elementary
+// Functions", 1980): k = the nearest integer to angle / (pi / 2), r = angle - k C1 - k C2 with pi / 2 split into
+// C1 = fp32(pi / 2) and C2 = fp32(pi / 2 - C1), each product exact inside its fma (the residual pi / 2 - C1 - C2,
+// about 2e-15, times k < 2^24 stays below 3e-8), so |r| <= pi / 4.  sin r and cos r come from their Taylor series
+// to the r^9 and r^10 terms (truncation error below 2e-9 on |r| <= pi / 4), and the quadrant k mod 4 turns
+// (cos r, sin r) by k quarter turns.  Absolute error about 1e-7 for pos < 2^24.
 __device__ __forceinline__ void rope_cos_sin(float pos, float th_hi, float th_lo, float& c, float& s) {
   const float a = pos * th_hi;
   const float d = fmaf(pos, th_lo, fmaf(pos, th_hi, -a));
-  float s0, c0;
-  sincosf(a, &s0, &c0);
-  s = fmaf(d, c0, s0);
-  c = fmaf(-d, s0, c0);
+  float k = rintf(a * 0.636619772367581343f);    // 2 / pi
+  float r = fmaf(-k, 1.57079637050628662f, a);         // C1
+  r = fmaf(-k, -4.37113882867379289e-8f, r) + d;
+  // Past 2^23 / (2 / pi) the product a (2 / pi) no longer resolves the fraction and k can be off by one: one more
+  // quarter turn brings r back to |r| <= pi / 4 (r -+ C1 is exact there).
+  if (r > 0.785398185f) {
+    k += 1.0f;
+    r = (r - 1.57079637050628662f) + 4.37113882867379289e-8f;
+  } else if (r < -0.785398185f) {
+    k -= 1.0f;
+    r = (r + 1.57079637050628662f) - 4.37113882867379289e-8f;
+  }      // C2
+  const float r2 = r * r;
+  float ps = fmaf(r2, 1.0f / 362880.0f, -1.0f / 5040.0f);   // sin r = r + r^3 (-1/3! + r^2 (1/5! + ...))
+  ps = fmaf(ps, r2, 1.0f / 120.0f);
+  ps = fmaf(ps, r2, -1.0f / 6.0f);
+  const float sr = fmaf(ps * r2, r, r);
+  float pc = fmaf(r2, -1.0f / 3628800.0f, 1.0f / 40320.0f);  // cos r = 1 + r^2 (-1/2! + r^2 (1/4! + ...))
+  pc = fmaf(pc, r2, -1.0f / 720.0f);
+  pc = fmaf(pc, r2, 1.0f / 24.0f);
+  pc = fmaf(pc, r2, -0.5f);
+  const float cr = fmaf(pc, r2, 1.0f);
+  const int quad = static_cast<int>(k) & 3;
+  const float c1 = (quad & 1) ? -sr : cr;   // a quarter turn: (cos, sin) -> (-sin, cos)
+  const float s1 = (quad & 1) ? cr : sr;
+  c = (quad & 2) ? -c1 : c1;                // a half turn: (cos, sin) -> (-cos, -sin)
+  s = (quad & 2) ? -s1 : s1;
 }
 
 }  // namespace nc

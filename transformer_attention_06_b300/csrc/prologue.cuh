@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(kPrologueThreads)
 //   * a sequence whose p0 is outside [0, Tcap - Tq] gets a zero output, its cache is left alone and the device
 //     status records NC_DEV_BAD_CACHE_LEN.
 // Blocks [0, n_tok_blocks) take one slice of a token per 8-lane group, the rest one row of a V tail copy per group.
-__global__ void __launch_bounds__(kPrologueThreads)
+// Two blocks per SM (at most 128 registers a thread), as for the full-prefill prologue.
+__global__ void __launch_bounds__(kPrologueThreads, 2)
     chunk_prologue_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
                           const __nv_bfloat16* __restrict__ v_new, __nv_bfloat16* __restrict__ qn,
                           __nv_bfloat16* kcache, __nv_bfloat16* vcache, __nv_bfloat16* __restrict__ vtail,
