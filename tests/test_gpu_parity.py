@@ -64,6 +64,33 @@ def test_prologue_rotation_is_accurate_at_large_positions(nc):
         assert err.max() <= 2.0 ** -17, f"worst excess over one ulp {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}"
 
 
+def test_prologue_rotation_is_accurate_up_to_position_2_24(nc):
+    """The largest positions the kernels take (T < 2^24), where the angle of the fastest pair exceeds 1.3e7 rad and
+    its fp32 reduction needs the extra quarter turn: 4096 sampled rows of a (2^24 - 1)-token sequence (the other rows
+    zero) carry seeded inputs, and each transformed row lies within one bf16 ulp of the fp64 oracle (plus 2^-17 near
+    zero)."""
+    T = (1 << 24) - 1
+    rng = np.random.default_rng(24)
+    rows = np.unique(np.concatenate([np.arange(T - 1024, T), rng.integers(1 << 23, T, 2048), rng.integers(0, T, 1024)]))
+    qs, ks, _ = fwd_inputs(1, len(rows), 1, 1, 128, seed=24)
+    dev = torch.device("cuda")
+    idx = torch.from_numpy(rows).to(dev)
+    qd = torch.zeros((1, T, 1, 128), dtype=torch.bfloat16, device=dev)
+    kd = torch.zeros_like(qd)
+    qd[0, idx] = qs[0].to(dev)
+    kd[0, idx] = ks[0].to(dev)
+    qn, kn = nc.nc_attn_qk_prologue(qd, kd)
+    torch.cuda.synchronize()
+    for got, x in ((qn, qs), (kn, ks)):
+        r = ref.qk_prologue(f64(x), rows[None, :])
+        g = f64(got[0, idx].cpu()[None])
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126))) - 7)
+        err = np.abs(g - r) - ulp
+        assert err.max() <= 2.0 ** -17, f"worst excess over one ulp {err.max():.3e}"
+    del qd, kd, qn, kn
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------------------------------------ prefill
 
 @pytest.mark.parametrize("W", TINY.windows)
